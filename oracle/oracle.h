@@ -1,0 +1,115 @@
+/*
+ * Q4_K / Q8_0 weight-only dequantize-and-multiply: the CPU ORACLE.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's
+ * CPU-baseline leg call this code.  The product path never links it and
+ * shares no code with it.
+ *
+ * Everything here is the plain definition, written for a reader to check by
+ * eye against the pages this project follows ("Mac Qwen3.6-27B Metal Q4_K perf
+ * diagnosis", TL;DR and section 4b; "Qwen3.6-27B on Apple M3 Pro -- the llama.cpp
+ * parity bar", model architecture and the reconciliation table):
+ *   dequantize every weight to f32, then accumulate the dot product in f64,
+ *   in index order.  No blocking, fusion or reordering.
+ *
+ * Q4_K byte layout (block_q4_K, 144 bytes per 256 weights, little-endian):
+ *   [0,2)   d     binary16        [2,4)   dmin  binary16
+ *   [4,16)  s[12] packed 6-bit scales sc_0..7 and mins m_0..7:
+ *             j<4 : sc_j = s[j] & 63,                 m_j = s[j+4] & 63
+ *             j>=4: sc_j = (s[j+4] & 15) | (s[j-4] >> 6) << 4
+ *                   m_j  = (s[j+4] >> 4) | (s[j]   >> 6) << 4
+ *   [16,144) qs[128]: qs[32g+l] low nibble = q of weight 64g+l,
+ *                      high nibble = q of weight 64g+32+l       (g<4, l<32)
+ *   weight i (sub-block j = i/32):  w = d*sc_j*q_i - dmin*m_j
+ * Q8_0 (block_q8_0, 34 bytes per 32 weights): binary16 d, then 32 int8 q; w = d*q.
+ *
+ * The quantizers (covering min/max for Q4_K, absmax for Q8_0) are the pinned
+ * readings listed in the design notes; the pages name the format only.
+ */
+#ifndef FAK_ORACLE_H
+#define FAK_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* binary16 helpers, written from IEEE 754-2008 (no library conversion). */
+float    orc_f16_decode(uint16_t h);
+uint16_t orc_f16_round_up(float v);   /* smallest binary16 >= v, for v >= 0; saturates at 65504 */
+uint16_t orc_f16_rne(float v);        /* round to nearest, ties to even; saturates at +-65504 */
+float    orc_bf16_decode(uint16_t b);
+
+/* Q4_K */
+void orc_q4k_quantize_superblock(const float* x256, uint8_t* out144);
+int  orc_q4k_pack(const float* w, int64_t N, int64_t K, uint8_t* out);   /* out: N*(K/256)*144 bytes */
+void orc_q4k_fields(const uint8_t* blk, uint16_t* d, uint16_t* dmin, uint8_t sc[8], uint8_t m[8],
+                    uint8_t q[256]);
+void orc_q4k_dequant_block(const uint8_t* blk, float* out256);
+void orc_q4k_dequant_rows(const uint8_t* W, int64_t N, int64_t K, float* out);
+
+/* Q8_0 */
+void orc_q8_0_quantize_block(const float* x32, uint8_t* out34);
+int  orc_q8_0_pack(const float* w, int64_t N, int64_t K, uint8_t* out);  /* out: N*(K/32)*34 bytes */
+void orc_q8_0_dequant_block(const uint8_t* blk, float* out32);
+
+/* y[n] = sum_k What[n,k]*x[k] in f64 (k ascending); a[n] = sum_k |What[n,k]*x[k]| (may be NULL). */
+void orc_gemv_q4k(const uint8_t* W, int64_t N, int64_t K, const float* x, double* y, double* a);
+void orc_gemv_q8_0(const uint8_t* W, int64_t N, int64_t K, const float* x, double* y, double* a);
+/* M independent GEMVs: Y[m,n], A[m,n] for X[m,:]. */
+void orc_gemv_batch_q4k(const uint8_t* W, int64_t N, int64_t K, const float* X, int64_t M,
+                        double* Y, double* A);
+/* Y[p,n] = sum_k What[n,k]*bf16(X[p,k]) in f64; X holds bfloat16 bit patterns. */
+void orc_gemm_q4k(const uint8_t* W, int64_t N, int64_t K, const uint16_t* X, int64_t P,
+                  double* Y, double* A);
+
+/* Y[i,j] = sum_k What[rows[j],k]*bf16(X[toks[i],k]) in f64 for sampled rows and tokens. */
+void orc_gemm_q4k_sample(const uint8_t* W, int64_t N, int64_t K, const uint16_t* X, int64_t P,
+                         const int64_t* rows, int64_t n_rows, const int64_t* toks, int64_t n_toks,
+                         double* Y, double* A);
+
+/* out = x / sqrt(mean(x^2) + eps), f64. */
+void orc_rmsnorm(const double* x, int64_t n, double eps, double* out);
+/* out = g / (1 + exp(-g)) * u, f64. */
+void orc_swiglu(const double* g, const double* u, int64_t n, double* out);
+/* index of the largest value; the lowest index wins ties; NaNs are skipped. */
+int64_t orc_argmax_f32(const float* v, int64_t n);
+
+/* ---- one decode token of the hybrid stack ---- */
+enum { ORC_LAYER_GDN = 0, ORC_LAYER_FA = 1 };
+typedef struct {
+    int32_t kind;
+    const uint8_t* w_in;    /* GDN in_proj / FA q+gate, [n_in x d_model] Q4_K */
+    const uint8_t* w_k;     /* FA only, [n_kv x d_model] */
+    const uint8_t* w_v;     /* FA only */
+    const uint8_t* w_out;   /* GDN out_proj / FA o, [d_model x n_mix] */
+    const uint8_t* w_gate;  /* [d_ff x d_model] */
+    const uint8_t* w_up;
+    const uint8_t* w_down;  /* [d_model x d_ff] */
+} orc_layer;
+typedef struct {
+    int64_t n_layers, d_model, d_ff, vocab;
+    int64_t gdn_in, fa_qg, fa_kv, n_mix;   /* in_proj rows, q+gate rows, k/v rows, mixer-out input width */
+    double eps;
+    const orc_layer* layers;
+    const uint8_t* lm_head;   /* [vocab x d_model] Q8_0 */
+    const float* embedding;   /* [vocab x d_model] f32 */
+} orc_model;
+/*
+ * h = E[tok]; per layer: n = rms(h); mixer projections; h += out(t[0:n_mix]);
+ * n = rms(h); h += down(swiglu(gate(n), up(n))).  Then logits = lm_head(rms(h)).
+ * h stays f64 between ops; each matmul input is rounded to f32 first.
+ * Outputs (each may be NULL): h_out[d_model] (final hidden, before the final
+ * norm), logits[vocab] (f32), logit_abs[vocab] (sum |w*x| per logit, for the
+ * tolerance), kv_out[n_layers/4 * 2 * fa_kv] (f32 k then v of each FA layer).
+ * Returns argmax(logits).
+ */
+int64_t orc_decode_token(const orc_model* m, int64_t tok, double* h_out, float* logits,
+                         double* logit_abs, float* kv_out);
+/* Raw bytes of weights one token streams (Q4_K matrices plus the Q8_0 lm_head). */
+int64_t orc_decode_weight_bytes(const orc_model* m);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
