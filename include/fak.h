@@ -1,0 +1,248 @@
+/*
+ * fak.h -- C ABI of the GB300 (sm_103a) Q4_K weight-only dequantize-and-multiply
+ * library (libfak.so).
+ *
+ * The method follows three pages about one engine ("fak"):
+ *   [diag]   "Mac Qwen3.6-27B Metal Q4_K perf diagnosis (2026-06-26)"
+ *   [parity] "Qwen3.6-27B on Apple M3 Pro -- the llama.cpp parity bar"
+ *   [prefill]"Qwen3.6-27B GDN-hybrid Metal prefill -- isolation split"
+ * The pages give the problem (a Q4_K GEMV per projection, a GEMV batch in one
+ * submission, a Q4_K prefill GEMM, and one GPU-resident submission per decode
+ * token); they name the Q4_K format but print no layout or kernel, so the
+ * byte layout below is the public GGML block_q4_K / block_q8_0 format.
+ *
+ * Conventions for every entry point:
+ *  - Returns a fak_status (0 = FAK_OK).  Nothing throws across the ABI.
+ *  - Shapes and alignment are validated on the host before any launch; a
+ *    failed validation launches nothing.
+ *  - "device" pointers are CUDA device (or managed) memory owned by the
+ *    caller; the library never frees them.  "host" pointers are ordinary host
+ *    memory owned by the caller.
+ *  - Device calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *    default stream) and never synchronize, unless stated.
+ *  - A launch error returns FAK_ERR_CUDA and clears the CUDA error state.
+ *  - Errors found on the device (a bounded wait that timed out, a token id
+ *    out of range) are written to a device status word and reported by
+ *    fak_device_status() / fak_decode_status().
+ *
+ * Matrix layout: a weight matrix W has N rows (outputs) and K columns
+ * (inputs), row-major, each row K/256 consecutive 144-byte Q4_K blocks
+ * (or K/32 consecutive 34-byte Q8_0 blocks).
+ *
+ * Q4_K block (144 B, 256 weights, little-endian): binary16 d at byte 0,
+ * binary16 dmin at byte 2, twelve bytes of packed 6-bit scales sc_0..7 and
+ * mins m_0..7 at bytes 4..15, then 128 bytes of 4-bit quants: byte 16+32g+l
+ * holds weight 64g+l in its low nibble and weight 64g+32+l in its high nibble.
+ * Weight i of sub-block j = i/32 is d*sc_j*q_i - dmin*m_j.
+ * Q8_0 block (34 B, 32 weights): binary16 d, then 32 int8 q; weight d*q.
+ */
+#ifndef FAK_H
+#define FAK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fak_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    FAK_OK = 0,
+    FAK_ERR_INVALID_ARG = 1, /* null pointer or bad enum value */
+    FAK_ERR_SHAPE = 2,       /* a dimension out of the supported range */
+    FAK_ERR_ALIGN = 3,       /* a pointer not 16-byte aligned */
+    FAK_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+    FAK_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up */
+    FAK_ERR_NOMEM = 6,       /* a workspace allocation failed */
+    FAK_ERR_DEVICE = 7,      /* the device rejected an input (e.g. token id out of range) */
+    FAK_ERR_UNSUPPORTED = 8  /* the current device is not sm_103 */
+} fak_status;
+
+/* Largest K (input length) the matrix-vector engine accepts: its quantized
+ * copy of x must fit in shared memory next to the weight ring. */
+#define FAK_ENGINE_MAX_K 18432
+
+/* Short English description of a status code (static storage). */
+const char* fak_strerror(int status);
+
+/* Library version string (static storage). */
+const char* fak_version(void);
+
+/* ------------------------------------------------------------------ packers
+ * Host-side quantizers ([diag] TL;DR and [parity] reconciliation table name
+ * raw q4_k blocks resident in memory; the quantizer itself is not on the
+ * pages: this is the covering min/max quantizer).
+ *
+ * fak_q4k_pack: w (host, f32, N x K row-major) -> out (host, N*(K/256)*144
+ * bytes).  Per 256-weight super-block and 32-weight sub-block j:
+ *   lo_j = min(0, min x), hi_j = max x, mn_j = -lo_j;
+ *   dmin = smallest binary16 >= max_j(mn_j)/63;  m_j = min(63, ceil(mn_j/dmin));
+ *   r_j = hi_j + dmin*m_j;  d = smallest binary16 >= max_j(r_j)/945;
+ *   sc_j = min(63, ceil(r_j/(15*d)));  q = clamp(rint((x + dmin*m_j)/(d*sc_j)), 0, 15)
+ * in f32 arithmetic (no fused multiply-add), 0 where a divisor is 0.  Every
+ * weight then round-trips within half a quant step d*sc_j/2.
+ * K % 256 != 0 or N < 0 -> FAK_ERR_SHAPE; out_bytes must equal the size.
+ * Multi-threaded; the bytes do not depend on the thread count.
+ *
+ * fak_q8_0_pack: w (host, f32, N x K) -> out (host, N*(K/32)*34 bytes).
+ *   d = binary16 nearest (ties to even) to max|x|/127;
+ *   q = clamp(rint(x/d), -127, 127), 0 if d == 0.   K % 32 != 0 -> FAK_ERR_SHAPE.
+ */
+int fak_q4k_pack(const float* w, int64_t N, int64_t K, void* out, size_t out_bytes);
+int fak_q8_0_pack(const float* w, int64_t N, int64_t K, void* out, size_t out_bytes);
+
+/* ------------------------------------------------------------------ GEMV
+ * y = W x for one activation vector ([diag] TL;DR: the Q4_K GEMV a decode
+ * token runs per projection; section 4b: the single-GEMV benchmark).
+ *   Wq: device, N rows of K/256 Q4_K blocks, 16-byte aligned.
+ *   x:  device f32 [K], 16-byte aligned.     y: device f32 [N].
+ *   1 <= N <= 2^31-1, 256 <= K <= FAK_ENGINE_MAX_K, K % 256 == 0.
+ * Accumulates exactly in integers per sub-block after splitting x into a
+ * 23-bit block-scaled fixed-point form (three byte limbs per element), then
+ * in f32; |error| stays within 1e-5 * sum|w_i x_i| + 1e-6 of the exact dot.
+ * Deterministic: the same inputs give bitwise identical y.
+ */
+int fak_q4k_gemv(const void* Wq, int64_t N, int64_t K, const float* x, float* y, fak_stream_t stream);
+
+/* Same for a Q8_0 matrix (the lm_head format of [diag] section 2, lm_head_q8).
+ * K % 256 == 0 (so rows stay 16-byte aligned), K <= FAK_ENGINE_MAX_K. */
+int fak_q8_0_gemv(const void* Wq, int64_t N, int64_t K, const float* x, float* y, fak_stream_t stream);
+
+/* ------------------------------------------------------------------ batched GEMV
+ * Y[m,:] = W X[m,:] for M activation rows against one resident weight
+ * ([diag] section 4b: GEMVBatch, N GEMVs of one weight in one submission).
+ *   X: device f32 [M, K] row-major, Y: device f32 [M, N]; 1 <= M <= 64.
+ *   Other limits and the error bound as fak_q4k_gemv.  W is read from HBM
+ *   once per call, not once per row.
+ */
+int fak_q4k_gemv_batch(const void* Wq, int64_t N, int64_t K, const float* X, int M, float* Y,
+                       fak_stream_t stream);
+
+/* ------------------------------------------------------------------ MLP decode
+ * One batch-1 SwiGLU MLP on Q4_K weights ([diag] section 2, mlp_decode, 54% of
+ * decode; [parity] architecture: RMSNorm eps 1e-6, SwiGLU):
+ *   n = x / sqrt(mean(x^2) + eps);  a = silu(Wgate n) * (Wup n);  y = Wdown a
+ * with unit RMSNorm gain.  Wgate, Wup: [d_ff x d_model]; Wdown: [d_model x d_ff].
+ *   x: device f32 [d_model]; y: device f32 [d_model] (may not alias x).
+ *   workspace: device, >= fak_mlp_workspace_bytes(d_ff) bytes, 256-byte
+ *   aligned, owned by the caller, not shared with a concurrent call.
+ * Runs as ONE kernel launch (both matmuls, the norm and SwiGLU inside, with a
+ * bounded grid-wide wait between them).
+ */
+size_t fak_mlp_workspace_bytes(int64_t d_ff);
+int fak_mlp_decode(const void* Wgate, const void* Wup, const void* Wdown, int64_t d_model, int64_t d_ff,
+                   const float* x, float eps, float* y, void* workspace, size_t workspace_bytes,
+                   fak_stream_t stream);
+
+/* ------------------------------------------------------------------ prefill GEMM
+ * Y = X W^T for P tokens ([diag] section 2: mlp_gate_up_proj and mlp_down_proj
+ * dominate prefill; section 4b: the q4k_gemm prefill kernel).
+ *   Wq: device Q4_K [N x K]; X: device bf16 [P, K] row-major (bit patterns);
+ *   Y: device f32 [P, N].  K % 256 == 0, N % 128 == 0, P >= 1.
+ * Tensor cores (tcgen05, bf16 x bf16 -> f32): W is dequantized to bf16 in
+ * shared memory, so |error| <= 5e-3 * sum|w_i x_i| + 1e-5.
+ */
+int fak_q4k_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, float* Y,
+                 fak_stream_t stream);
+
+/* Elementwise X2[p, i] = bf16(silu(Y1[p, i]) * Y1[p, half + i]) for i < half:
+ * the SwiGLU between the fused gate||up prefill GEMM and the down GEMM.
+ * Y1: device f32 [P, 2*half]; X2: device bf16 [P, half]. */
+int fak_swiglu_bf16(const float* Y1, int64_t P, int64_t half, void* X2, fak_stream_t stream);
+
+/* ------------------------------------------------------------------ decode step
+ * One decode token of the hybrid stack as ONE launch ([diag] section 4, the
+ * "one-command-buffer-per-token GPU-resident decode forward": the activation
+ * stays on the GPU across every projection and MLP matmul, one submission
+ * per token).  Per token:
+ *   h = E[tok]; for each layer: n = rms(h);
+ *     GDN layer: t = Win n; h += Wout t[0:n_mix]
+ *     FA  layer: t = Wqg n; k = Wk n; v = Wv n; h += Wo t[0:n_mix]
+ *   (the mixer bodies between the projections are outside this library);
+ *   n = rms(h); h += Wdown(silu(Wgate n) * (Wup n));
+ *   finally logits = Wlm rms(h) (Q8_0) and tok' = argmax(logits), lowest
+ *   index on ties.  RMSNorm gain is 1.
+ */
+enum { FAK_LAYER_GDN = 0, FAK_LAYER_FA = 1 };
+enum { FAK_DECODE_ONE_LAUNCH = 0, FAK_DECODE_PER_MATMUL = 1 };
+
+typedef struct {
+    int32_t kind;          /* FAK_LAYER_GDN or FAK_LAYER_FA */
+    const void* w_in;      /* GDN in_proj [gdn_in x d_model] / FA q+gate [fa_qg x d_model], Q4_K, device */
+    const void* w_k;       /* FA only: [fa_kv x d_model] Q4_K, device (NULL for GDN) */
+    const void* w_v;       /* FA only */
+    const void* w_out;     /* GDN out_proj / FA o: [d_model x n_mix] Q4_K, device */
+    const void* w_gate;    /* [d_ff x d_model] Q4_K, device */
+    const void* w_up;      /* [d_ff x d_model] */
+    const void* w_down;    /* [d_model x d_ff] */
+} fak_layer_desc;
+
+typedef struct {
+    int32_t n_layers;
+    int32_t d_model, d_ff, vocab;
+    int32_t gdn_in, fa_qg, fa_kv, n_mix;
+    float eps;
+    int32_t mode;                 /* FAK_DECODE_ONE_LAUNCH or FAK_DECODE_PER_MATMUL */
+    const fak_layer_desc* layers; /* host array of n_layers; copied by fak_decode_create */
+    const void* lm_head;          /* [vocab x d_model] Q8_0, device */
+    const float* embedding;       /* [vocab x d_model] f32, device */
+} fak_decode_desc;
+
+typedef struct fak_decode fak_decode;
+
+/* Validates the description and allocates the context's device scratch
+ * (hidden state, projection outputs, k/v outputs, SwiGLU output, argmax
+ * candidates, sync counters, status word, the op list).  The weights stay
+ * owned by the caller and must outlive the context.  Limits: d_model,
+ * n_mix, d_ff <= FAK_ENGINE_MAX_K and multiples of 256; n_mix <= max(gdn_in,
+ * fa_qg).  ONE_LAUNCH needs a device that can co-schedule one block per SM. */
+int fak_decode_create(const fak_decode_desc* desc, fak_decode** out);
+
+/* One token: reads d_tok_in (device int32), writes d_tok_out (device int32;
+ * may equal d_tok_in), and, if d_logits (device f32 [vocab]) is not NULL,
+ * the logits.  Asynchronous; ONE_LAUNCH issues a single kernel launch,
+ * PER_MATMUL one launch per matmul (same arithmetic, bitwise identical
+ * results).  Returns a status left on the device by an earlier step without
+ * synchronizing (it reads the status word only after a previous
+ * fak_decode_status). */
+int fak_decode_step(fak_decode* ctx, const int32_t* d_tok_in, int32_t* d_tok_out, float* d_logits,
+                    fak_stream_t stream);
+
+/* Synchronizes `stream`, reads and clears the context's device status word:
+ * FAK_OK, FAK_ERR_TIMEOUT (a grid-wide wait gave up; the counters are reset
+ * so the context stays usable) or FAK_ERR_DEVICE (token id out of range). */
+int fak_decode_status(fak_decode* ctx, fak_stream_t stream);
+
+/* Copies part of the context's state after a step into dst (host or device
+ * memory, caller-owned), stream-ordered on `stream`:
+ *   which = 0: the hidden state h [d_model] (before the final norm);
+ *   which = 1: the k and v projections of every FA layer, [n_fa][2][fa_kv].
+ * `count` must equal the number of floats of that buffer. */
+int fak_decode_read_state(fak_decode* ctx, int which, float* dst, size_t count, fak_stream_t stream);
+
+/* Number of kernel launches one fak_decode_step issues. */
+int fak_decode_launches_per_step(const fak_decode* ctx);
+
+/* Test hook: the grid-wide wait timeout in nanoseconds (default 1 s).  A
+ * step whose wait cannot complete within it returns early with
+ * FAK_ERR_TIMEOUT in the status word instead of hanging. */
+int fak_decode_set_timeout_ns(fak_decode* ctx, int64_t ns);
+
+/* Test hook: make op `op_index` of the next step wait for one more arrival
+ * than the grid can provide (a wait that can never complete), to check the
+ * bounded-wait error path.  -1 clears it. */
+int fak_decode_debug_unreachable_wait(fak_decode* ctx, int op_index);
+
+void fak_decode_destroy(fak_decode* ctx);
+
+/* ------------------------------------------------------------------ status
+ * Synchronizes `stream`, then reads and clears the status word shared by the
+ * stateless calls (GEMV, batched GEMV, MLP, GEMM). */
+int fak_device_status(fak_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FAK_H */

@@ -1,0 +1,970 @@
+// The matrix-vector engine: Q4_K / Q8_0 weight-streaming GEMV on sm_103a, and
+// a list of such matvecs (with RMSNorm on the input, SwiGLU / residual-add /
+// argmax epilogues) run as ONE persistent launch with bounded grid-wide waits
+// between dependent steps.
+//
+// What it computes follows "Mac Qwen3.6-27B Metal Q4_K perf diagnosis": the
+// per-projection Q4_K GEMV (TL;DR), the lm_head_q8 matvec (section 2 profile)
+// and the one-submission-per-token decode forward (section 4, "the lever"),
+// where the activation stays on the GPU across every matmul of a token.
+//
+// Design (GB300-first):
+//  * One CTA per SM: 1 producer warp + 8 consumer warps, ~217 KB shared memory.
+//  * The producer streams each CTA's weight rows HBM -> shared memory with
+//    cp.async.bulk into a 16-slot ring (9 KB slots: 8 rows x 8 Q4_K blocks,
+//    or 8 rows x 32 Q8_0 blocks) completing on mbarriers.  It never waits for
+//    activations, so in a multi-step launch it prefetches the next matmul's
+//    weights while the grid waits for the previous step's output.
+//  * Consumers quantize x once per step into shared memory: per 256-element
+//    super-block a power-of-two scale s with |x/s| <= 2^22, X = rint(x/s) split
+//    into three byte limbs (X = X2*65536 + X1*256 + X0, X0/X1 unsigned, X2
+//    signed).  The dot over each 32-weight sub-block is then exact integer
+//    arithmetic (DP4A on 4-bit quants x byte limbs); the sub-block scales sc_j
+//    are applied in integers, and one f32 conversion per block follows.
+//    Relative to f32 activations this adds at most 2^-23 * max|x| per element
+//    of its super-block.
+//  * Each weight row group (8 rows) is owned by one consumer warp; lanes cover
+//    (block, 64-weight group) pairs so x limbs in registers serve all 8 rows.
+//    Row results are reduced with a fixed shuffle tree: bitwise deterministic.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "fak.h"
+#include "fak_device.cuh"
+
+namespace {
+
+constexpr int kNumConsumerWarps = 8;
+constexpr int kThreads = 32 * (kNumConsumerWarps + 1);
+constexpr int kConsumerThreads = 32 * kNumConsumerWarps;
+constexpr int kStages = 16;
+constexpr int kStageBytes = 9216;        // 8 rows x 8 Q4_K blocks x 144 B
+constexpr int kRowsPerGroup = 8;
+constexpr int kQ4SlabBlocks = 8;         // Q4_K blocks per row per stage
+constexpr int kQ8SlabBlocks = 32;        // Q8_0 blocks per row per stage
+constexpr int kQ4StageRow = kQ4SlabBlocks * 144;  // 1152
+constexpr int kQ8StageRow = kQ8SlabBlocks * 34;   // 1088
+constexpr int kMaxSuper = FAK_ENGINE_MAX_K / 256; // 72
+constexpr int kRecBytes = 112;           // one 32-element record: 3 x 32 limb bytes + 16 pad
+constexpr int kSuperBytes = 8 * kRecBytes + 16;   // 912: padding keeps lane accesses conflict-free
+
+constexpr int kOffRing = 0;
+constexpr int kOffX = kOffRing + kStages * kStageBytes;           // 147456
+constexpr int kOffS = kOffX + kMaxSuper * kSuperBytes;            // +65664
+constexpr int kOffScale = kOffS + kMaxSuper * 8 * 4;
+constexpr int kOffBar = kOffScale + kMaxSuper * 4;
+constexpr int kOffMisc = kOffBar + 2 * kStages * 8;
+constexpr int kSmemBytes = kOffMisc + 256;
+constexpr int kSmemAlloc = kSmemBytes + 128;
+
+enum OpKind { OP_Q4K = 0, OP_Q4K_SWIGLU = 1, OP_Q8 = 2, OP_EMBED = 3, OP_ARGMAX_REDUCE = 4 };
+enum OpFlag { F_NORM = 1, F_RESID = 2, F_WAIT = 4, F_ARGMAX = 8 };
+
+struct EngOp {
+  int32_t kind, flags, K, nseg;
+  int32_t wait_extra, vocab;
+  int64_t nrows;            // output rows (SWIGLU: rows of gate = rows of up)
+  int64_t seg_end[3];       // cumulative row ends per segment
+  const uint8_t* w[3];      // weights per segment (SWIGLU: w[0] gate, w[1] up)
+  float* y[3];              // outputs per segment
+  const float* x;           // input vector [K] (EMBED: the embedding table)
+  float eps;
+  int32_t pad;
+};
+
+struct EngParams {
+  const EngOp* ops;         // device array, or NULL to use inl[]
+  int n_ops;
+  int first_wait;
+  unsigned* sync;           // [0] steps done (sum over CTAs), [1] CTAs exited; NULL: no grid waits
+  int* err;
+  float* cand_val;
+  int* cand_idx;
+  const int* tok_in;
+  int* tok_out;
+  float* logits;
+  unsigned long long timeout_ns;
+  EngOp inl[2];             // used when ops == NULL (at most 2 steps)
+};
+
+__device__ int g_fak_status;  // status word of the stateless entry points
+
+__device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+struct Geo {
+  int U;          // output rows per group
+  int bpr;        // blocks per row
+  int slab;       // blocks per row per stage
+  int nslab;
+  int blk;        // bytes per block
+  int srow;       // bytes between row slots in a stage
+  bool pair, q8;
+};
+
+__device__ __forceinline__ Geo geo_of(const EngOp& op) {
+  Geo g;
+  g.q8 = op.kind == OP_Q8;
+  g.pair = op.kind == OP_Q4K_SWIGLU;
+  g.U = g.pair ? 4 : kRowsPerGroup;
+  g.bpr = g.q8 ? op.K / 32 : op.K / 256;
+  g.slab = g.q8 ? kQ8SlabBlocks : kQ4SlabBlocks;
+  g.nslab = (g.bpr + g.slab - 1) / g.slab;
+  g.blk = g.q8 ? 34 : 144;
+  g.srow = g.q8 ? kQ8StageRow : kQ4StageRow;
+  return g;
+}
+
+__device__ __forceinline__ bool has_weights(int kind) {
+  return kind == OP_Q4K || kind == OP_Q4K_SWIGLU || kind == OP_Q8;
+}
+
+__device__ __forceinline__ void group_range(int64_t ngroups, int64_t& g0, int64_t& g1) {
+  const int64_t c = blockIdx.x, G = gridDim.x;
+  g0 = ngroups * c / G;
+  g1 = ngroups * (c + 1) / G;
+}
+
+__device__ __forceinline__ void set_error(const EngParams& P, int code, volatile int* abort) {
+  int* e = P.err ? P.err : &g_fak_status;
+  atomicCAS(e, 0, code);
+  *abort = 1;
+}
+
+// ------------------------------------------------------------------ producer
+__device__ void producer(const EngParams& P, uint8_t* smem, uint64_t* full, uint64_t* empty, volatile int* abort,
+                         int* issued_out) {
+  const uint64_t pol = l2_evict_first_policy();
+  int q = 0;
+  for (int i = 0; i < P.n_ops && !*abort; ++i) {
+    const EngOp& op = P.ops ? P.ops[i] : P.inl[i];
+    if (!has_weights(op.kind)) continue;
+    const Geo g = geo_of(op);
+    const int64_t ngroups = (op.nrows + g.U - 1) / g.U;
+    int64_t g0, g1;
+    group_range(ngroups, g0, g1);
+    const int64_t row_bytes = (int64_t)g.bpr * g.blk;
+    for (int64_t wv = g0; wv < g1; wv += kNumConsumerWarps) {
+      const int nw = (int)imin64(kNumConsumerWarps, g1 - wv);
+      for (int s = 0; s < g.nslab; ++s) {
+        const int nb = min(g.slab, g.bpr - s * g.slab);
+        const uint32_t bytes_row = (uint32_t)(nb * g.blk);
+        for (int k = 0; k < nw; ++k, ++q) {
+          const int slot = q % kStages;
+          const int use = q / kStages;
+          if (use > 0 && !mbar_wait_bounded(&empty[slot], (use - 1) & 1, abort, P.timeout_ns)) {
+            if (!*abort) set_error(P, FAK_ERR_TIMEOUT, abort);
+            *issued_out = q;
+            return;
+          }
+          const int64_t r0 = (wv + k) * g.U;
+          const int nr = (int)imin64(g.U, op.nrows - r0);
+          uint8_t* stage = smem + kOffRing + slot * kStageBytes;
+          mbar_arrive_expect_tx(&full[slot], bytes_row * nr * (g.pair ? 2 : 1));
+          for (int rl = 0; rl < nr; ++rl) {
+            const int64_t row = r0 + rl;
+            if (g.pair) {
+              const int64_t off = row * row_bytes + (int64_t)s * g.slab * g.blk;
+              bulk_g2s(stage + rl * g.srow, op.w[0] + off, bytes_row, &full[slot], pol);
+              bulk_g2s(stage + (4 + rl) * g.srow, op.w[1] + off, bytes_row, &full[slot], pol);
+            } else {
+              int seg = 0;
+              int64_t seg_start = 0;
+              while (seg < op.nseg - 1 && row >= op.seg_end[seg]) seg_start = op.seg_end[seg++];
+              const uint8_t* src = op.w[seg] + (row - seg_start) * row_bytes + (int64_t)s * g.slab * g.blk;
+              bulk_g2s(stage + rl * g.srow, src, bytes_row, &full[slot], pol);
+            }
+          }
+        }
+      }
+    }
+  }
+  *issued_out = q;
+}
+
+// ------------------------------------------------------------------ x preparation
+// Quantize x (optionally RMS-normalized) into the limb records in shared memory.
+__device__ void prepare_x(const EngOp& op, uint8_t* smem, float* red, int cw, int lane, int ctid) {
+  const int K = op.K;
+  const float* x = op.x;
+  float rn = 1.0f;
+  if (op.flags & F_NORM) {
+    float ss = 0.0f;
+    for (int i = ctid * 4; i < K; i += kConsumerThreads * 4) {
+      float4 v = ld_cg_f4(x + i);
+      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) red[cw] = ss;
+    named_bar_sync(1, kConsumerThreads);
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kNumConsumerWarps; ++w) tot += red[w];
+    rn = 1.0f / sqrtf(tot / (float)K + op.eps);
+  }
+  uint8_t* xq = smem + kOffX;
+  float* xS = reinterpret_cast<float*>(smem + kOffS);
+  float* xsc = reinterpret_cast<float*>(smem + kOffScale);
+  const int nsb = K / 256;
+  for (int sb = cw; sb < nsb; sb += kNumConsumerWarps) {
+    const float* src = x + sb * 256 + lane * 8;
+    float4 a = ld_cg_f4(src), b = ld_cg_f4(src + 4);
+    float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float am = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[i] *= rn;
+      am = fmaxf(am, fabsf(v[i]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    const uint32_t eb = (__float_as_uint(am) >> 23) & 0xFF;  // am in [2^(eb-127), 2^(eb-126))
+    float f = 0.0f, sx = 0.0f;
+    if (eb >= 22) {
+      f = __uint_as_float((275u - eb) << 23);  // 2^(148-eb): |v*f| < 2^22
+      sx = __uint_as_float((eb - 21u) << 23);  // 1/f
+    }
+    int X[8];
+    int xsum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      X[i] = __float2int_rn(v[i] * f);
+      xsum += X[i];
+    }
+    uint32_t p0[2], p1[2], p2[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      p0[h] = p1[h] = p2[h] = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int xi = X[4 * h + i];
+        p0[h] |= (uint32_t)(xi & 255) << (8 * i);
+        p1[h] |= (uint32_t)((xi >> 8) & 255) << (8 * i);
+        p2[h] |= (uint32_t)((xi >> 16) & 255) << (8 * i);
+      }
+    }
+    uint8_t* rec = xq + sb * kSuperBytes + (lane >> 2) * kRecBytes + (lane & 3) * 8;
+    *reinterpret_cast<uint2*>(rec) = make_uint2(p0[0], p0[1]);
+    *reinterpret_cast<uint2*>(rec + 32) = make_uint2(p1[0], p1[1]);
+    *reinterpret_cast<uint2*>(rec + 64) = make_uint2(p2[0], p2[1]);
+    xsum += __shfl_xor_sync(0xffffffffu, xsum, 1);
+    xsum += __shfl_xor_sync(0xffffffffu, xsum, 2);
+    if ((lane & 3) == 0) xS[sb * 8 + (lane >> 2)] = sx * (float)xsum;
+    if (lane == 0) xsc[sb] = sx;
+  }
+}
+
+// ------------------------------------------------------------------ Q4_K slab
+// One stage: up to 8 rows x up to 8 blocks.  Lane (b, g) = (lane/4, lane%4)
+// covers block b of the slab and its 64-weight group g (sub-blocks 2g, 2g+1).
+__device__ __forceinline__ void q4k_slab(const uint8_t* stage, const uint8_t* smem, int jb0, int nb, uint32_t rowmask,
+                                         int lane, float acc[8]) {
+  const int b = lane >> 2, g = lane & 3;
+  if (b >= nb) return;
+  const int jb = jb0 + b;
+  const uint8_t* rec = smem + kOffX + jb * kSuperBytes + (2 * g) * kRecBytes;
+  const uint4* r0 = reinterpret_cast<const uint4*>(rec);
+  const uint4* r1 = reinterpret_cast<const uint4*>(rec + kRecBytes);
+  uint32_t A0w[8], A1w[8], A2w[8], B0w[8], B1w[8], B2w[8];
+  {
+    uint4 t;
+    t = r0[0]; A0w[0] = t.x; A0w[1] = t.y; A0w[2] = t.z; A0w[3] = t.w;
+    t = r0[1]; A0w[4] = t.x; A0w[5] = t.y; A0w[6] = t.z; A0w[7] = t.w;
+    t = r0[2]; A1w[0] = t.x; A1w[1] = t.y; A1w[2] = t.z; A1w[3] = t.w;
+    t = r0[3]; A1w[4] = t.x; A1w[5] = t.y; A1w[6] = t.z; A1w[7] = t.w;
+    t = r0[4]; A2w[0] = t.x; A2w[1] = t.y; A2w[2] = t.z; A2w[3] = t.w;
+    t = r0[5]; A2w[4] = t.x; A2w[5] = t.y; A2w[6] = t.z; A2w[7] = t.w;
+    t = r1[0]; B0w[0] = t.x; B0w[1] = t.y; B0w[2] = t.z; B0w[3] = t.w;
+    t = r1[1]; B0w[4] = t.x; B0w[5] = t.y; B0w[6] = t.z; B0w[7] = t.w;
+    t = r1[2]; B1w[0] = t.x; B1w[1] = t.y; B1w[2] = t.z; B1w[3] = t.w;
+    t = r1[3]; B1w[4] = t.x; B1w[5] = t.y; B1w[6] = t.z; B1w[7] = t.w;
+    t = r1[4]; B2w[0] = t.x; B2w[1] = t.y; B2w[2] = t.z; B2w[3] = t.w;
+    t = r1[5]; B2w[4] = t.x; B2w[5] = t.y; B2w[6] = t.z; B2w[7] = t.w;
+  }
+  const float* xS = reinterpret_cast<const float*>(smem + kOffS);
+  const float SA = xS[jb * 8 + 2 * g], SB = xS[jb * 8 + 2 * g + 1];
+  const float sx16 = reinterpret_cast<const float*>(smem + kOffScale)[jb] * 0.0625f;
+  const uint32_t sel = (uint32_t)(2 * g) | ((uint32_t)(2 * g + 1) << 4);
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    if (!((rowmask >> r) & 1)) continue;
+    const uint8_t* base = stage + r * kQ4StageRow + b * 144;
+    const uint4 h = *reinterpret_cast<const uint4*>(base);
+    const uint4 qa = *reinterpret_cast<const uint4*>(base + 16 + 32 * g);
+    const uint4 qb = *reinterpret_cast<const uint4*>(base + 32 + 32 * g);
+    const uint32_t sc_lo = h.y & 0x3F3F3F3Fu;
+    const uint32_t m_lo = h.z & 0x3F3F3F3Fu;
+    const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
+    const uint32_t m_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+    const uint32_t scp = prmt(sc_lo, sc_hi, sel);
+    const uint32_t mp = prmt(m_lo, m_hi, sel);
+    const int scA16 = (int)(scp & 0xFF) << 4, scB = (int)((scp >> 8) & 0xFF);
+    const float mA = (float)(mp & 0xFF), mB = (float)((mp >> 8) & 0xFF);
+    const float d = half_bits_to_float(h.x & 0xFFFF), dmin = half_bits_to_float(h.x >> 16);
+    const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    uint32_t a0 = 0, a1 = 0, b0 = 0, b1 = 0;
+    int a2 = 0, b2 = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t lo = w[u] & 0x0F0F0F0Fu, hi = w[u] & 0xF0F0F0F0u;
+      a0 = dp4a_uu(lo, A0w[u], a0);
+      a1 = dp4a_uu(lo, A1w[u], a1);
+      a2 = dp4a_us(lo, A2w[u], a2);
+      b0 = dp4a_uu(hi, B0w[u], b0);
+      b1 = dp4a_uu(hi, B1w[u], b1);
+      b2 = dp4a_us(hi, B2w[u], b2);
+    }
+    const int J0 = (int)a0 * scA16 + (int)b0 * scB;
+    const int J1 = (int)a1 * scA16 + (int)b1 * scB;
+    const int J2 = a2 * scA16 + b2 * scB;
+    const float Jf = fmaf((float)J2, 65536.0f, fmaf((float)J1, 256.0f, (float)J0));
+    const float mterm = fmaf(mA, SA, mB * SB);
+    acc[r] = fmaf(d * sx16, Jf, fmaf(-dmin, mterm, acc[r]));
+  }
+}
+
+// ------------------------------------------------------------------ Q8_0 slab
+// One stage: up to 8 rows x up to 32 blocks; lane l covers block l.
+__device__ __forceinline__ void q8_slab(const uint8_t* stage, const uint8_t* smem, int cb0, int nb, uint32_t rowmask,
+                                        int lane, float acc[8]) {
+  if (lane >= nb) return;
+  const int cb = cb0 + lane;
+  const uint4* rec = reinterpret_cast<const uint4*>(smem + kOffX + (cb >> 3) * kSuperBytes + (cb & 7) * kRecBytes);
+  uint32_t P0[8], P1[8], P2[8];
+  {
+    uint4 t;
+    t = rec[0]; P0[0] = t.x; P0[1] = t.y; P0[2] = t.z; P0[3] = t.w;
+    t = rec[1]; P0[4] = t.x; P0[5] = t.y; P0[6] = t.z; P0[7] = t.w;
+    t = rec[2]; P1[0] = t.x; P1[1] = t.y; P1[2] = t.z; P1[3] = t.w;
+    t = rec[3]; P1[4] = t.x; P1[5] = t.y; P1[6] = t.z; P1[7] = t.w;
+    t = rec[4]; P2[0] = t.x; P2[1] = t.y; P2[2] = t.z; P2[3] = t.w;
+    t = rec[5]; P2[4] = t.x; P2[5] = t.y; P2[6] = t.z; P2[7] = t.w;
+  }
+  const float sx = reinterpret_cast<const float*>(smem + kOffScale)[cb >> 3];
+  const int odd = lane & 1;  // 34*lane % 4 == 2*odd: odd lanes have aligned quants
+  const uint32_t sel = odd ? 0x7654u : 0x5432u;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    if (!((rowmask >> r) & 1)) continue;
+    const uint32_t* wp = reinterpret_cast<const uint32_t*>(stage + r * kQ8StageRow + ((34 * lane) & ~3));
+    uint32_t w[9];
+#pragma unroll
+    for (int u = 0; u < 9; ++u) w[u] = wp[u];
+    const float d = half_bits_to_float(odd ? (w[0] >> 16) : (w[0] & 0xFFFF));
+    int i0 = 0, i1 = 0, i2 = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t q = prmt(w[u], w[u + 1], sel);
+      i0 = dp4a_su(q, P0[u], i0);
+      i1 = dp4a_su(q, P1[u], i1);
+      i2 = dp4a_ss(q, P2[u], i2);
+    }
+    const float Jf = fmaf((float)i2, 65536.0f, fmaf((float)i1, 256.0f, (float)i0));
+    acc[r] = fmaf(d * sx, Jf, acc[r]);
+  }
+}
+
+__device__ __forceinline__ void better(float v, int idx, float& bv, int& bi) {
+  if (idx < 0 || v != v) return;
+  if (bi < 0 || v > bv || (v == bv && idx < bi)) {
+    bv = v;
+    bi = idx;
+  }
+}
+
+// ------------------------------------------------------------------ consumers
+__device__ void consumers(const EngParams& P, uint8_t* smem, uint64_t* full, uint64_t* empty, volatile int* abort) {
+  const int ctid = threadIdx.x - 32;
+  const int cw = ctid >> 5, lane = ctid & 31;
+  float* red = reinterpret_cast<float*>(smem + kOffMisc);          // [8]
+  float* bestv = red + 8;                                           // [8]
+  int* besti = reinterpret_cast<int*>(red + 16);                    // [8]
+  int q_base = 0;
+  const unsigned G = gridDim.x;
+  for (int i = 0; i < P.n_ops; ++i) {
+    const EngOp& op = P.ops ? P.ops[i] : P.inl[i];
+    // -- wait for the previous step of this launch to finish on every CTA
+    if (ctid == 0 && P.sync && (op.flags & F_WAIT) && (i > 0 || P.first_wait) && !*abort) {
+      const unsigned target = (unsigned)i * G + (unsigned)op.wait_extra;
+      if (ld_acquire_gpu(&P.sync[0]) < target) {
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(&P.sync[0]) < target) {
+          __nanosleep(32);
+          if (globaltimer_ns() - t0 > P.timeout_ns) {
+            set_error(P, FAK_ERR_TIMEOUT, abort);
+            break;
+          }
+        }
+      }
+    }
+    named_bar_sync(1, kConsumerThreads);
+    if (*abort) break;
+
+    if (op.kind == OP_EMBED) {
+      int tok = P.tok_in ? *P.tok_in : 0;
+      if (tok < 0 || tok >= op.vocab) {
+        if (ctid == 0) atomicCAS(P.err ? P.err : &g_fak_status, 0, FAK_ERR_DEVICE);
+        tok = 0;
+      }
+      const int64_t D = op.K, c = blockIdx.x;
+      const int64_t a = D * c / G, b = D * (c + 1) / G;
+      for (int64_t k = a + ctid; k < b; k += kConsumerThreads) op.y[0][k] = op.x[(int64_t)tok * D + k];
+    } else if (op.kind == OP_ARGMAX_REDUCE) {
+      if (blockIdx.x == 0 && cw == 0) {
+        float bv = 0.0f;
+        int bi = -1;
+        for (unsigned c = lane; c < G; c += 32) better(ld_cg_f(P.cand_val + c), ld_cg_i(P.cand_idx + c), bv, bi);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          better(ov, oi, bv, bi);
+        }
+        if (lane == 0 && P.tok_out) *P.tok_out = bi < 0 ? 0 : bi;
+      }
+    } else {
+      prepare_x(op, smem, red, cw, lane, ctid);
+      named_bar_sync(1, kConsumerThreads);
+      const Geo g = geo_of(op);
+      const int64_t ngroups = (op.nrows + g.U - 1) / g.U;
+      int64_t g0, g1;
+      group_range(ngroups, g0, g1);
+      float wbv = 0.0f;
+      int wbi = -1;
+      for (int64_t wv = g0; wv < g1; wv += kNumConsumerWarps) {
+        const int nw = (int)imin64(kNumConsumerWarps, g1 - wv);
+        if (cw < nw && !*abort) {
+          const int64_t r0 = (wv + cw) * g.U;
+          const int nr = (int)imin64(g.U, op.nrows - r0);
+          const uint32_t rowmask = g.pair ? (((1u << nr) - 1) * 0x11u) : ((1u << nr) - 1);
+          float acc[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
+          const int qw = q_base + (int)(wv - g0) * g.nslab;
+          for (int s = 0; s < g.nslab; ++s) {
+            const int q = qw + s * nw + cw;
+            const int slot = q % kStages;
+            if (!mbar_wait_bounded(&full[slot], (q / kStages) & 1, abort, P.timeout_ns)) {
+              if (!*abort) set_error(P, FAK_ERR_TIMEOUT, abort);
+              break;
+            }
+            const uint8_t* stage = smem + kOffRing + slot * kStageBytes;
+            const int nb = min(g.slab, g.bpr - s * g.slab);
+            if (g.q8)
+              q8_slab(stage, smem, s * g.slab, nb, rowmask, lane, acc);
+            else
+              q4k_slab(stage, smem, s * g.slab, nb, rowmask, lane, acc);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+          }
+          // fixed butterfly: every lane ends with the same-order-per-lane totals
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+          }
+          if (g.pair) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              if (lane == r && r < nr) {
+                const float gt = acc[r], up = acc[4 + r];
+                op.y[0][r0 + r] = gt / (1.0f + expf(-gt)) * up;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              if (lane == r && r < nr) {
+                const int64_t row = r0 + r;
+                int seg = 0;
+                int64_t seg_start = 0;
+                while (seg < op.nseg - 1 && row >= op.seg_end[seg]) seg_start = op.seg_end[seg++];
+                float* yp = op.y[seg] + (row - seg_start);
+                float v = acc[r];
+                if (op.flags & F_RESID) v += ld_cg_f(yp);
+                if (op.flags & F_ARGMAX) {
+                  if (P.logits) P.logits[row] = v;
+                } else {
+                  *yp = v;
+                }
+              }
+            }
+            if (op.flags & F_ARGMAX) {
+#pragma unroll
+              for (int r = 0; r < 8; ++r)
+                if (r < nr) better(acc[r], (int)(r0 + r), wbv, wbi);
+            }
+          }
+        }
+      }
+      q_base += (int)(g1 - g0) * g.nslab;
+      if (op.flags & F_ARGMAX) {
+        if (lane == 0) {
+          bestv[cw] = wbv;
+          besti[cw] = wbi;
+        }
+        named_bar_sync(1, kConsumerThreads);
+        if (ctid == 0) {
+          float bv = 0.0f;
+          int bi = -1;
+          for (int w = 0; w < kNumConsumerWarps; ++w) better(bestv[w], besti[w], bv, bi);
+          P.cand_val[blockIdx.x] = bv;
+          P.cand_idx[blockIdx.x] = bi;
+        }
+      }
+    }
+    // -- this CTA finished step i
+    named_bar_sync(1, kConsumerThreads);
+    if (ctid == 0 && P.sync) {
+      __threadfence();
+      atomicAdd(&P.sync[0], 1u);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_constant__ EngParams P) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* empty = full + kStages;
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 96);
+  int* issued = reinterpret_cast<int*>(smem + kOffMisc + 100);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    *abort = 0;
+    *issued = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    if (threadIdx.x == 0) {
+      producer(P, smem, full, empty, abort, issued);
+      if (*abort) {
+        // let every copy this CTA issued land before the CTA exits
+        const int q1 = *issued;
+        for (int q = max(0, q1 - kStages); q < q1; ++q) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&full[q % kStages], (q / kStages) & 1))
+            if (globaltimer_ns() - t0 > 100000000ull) break;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    consumers(P, smem, full, empty, abort);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && P.sync) {
+    __threadfence();
+    const unsigned prev = atomicAdd(&P.sync[1], 1u);
+    if (prev == gridDim.x - 1) {
+      atomicExch(&P.sync[0], 0u);
+      atomicExch(&P.sync[1], 0u);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host side
+struct DeviceInfo {
+  int sms = 0;
+  bool ok = false;
+  bool attr_set = false;
+};
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+
+int device_setup(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fak_cuda_status(cudaErrorInvalidDevice);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.attr_set) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (major != 10 || minor != 3) return FAK_ERR_UNSUPPORTED;
+    cudaError_t e = cudaFuncSetAttribute(engine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (e != cudaSuccess) return fak_cuda_status(e);
+    di.attr_set = true;
+    di.ok = true;
+  }
+  *sms = di.sms;
+  return FAK_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+EngOp make_matvec(int kind, const void* W, int64_t N, int64_t K, const float* x, float* y, int flags) {
+  EngOp op;
+  memset(&op, 0, sizeof(op));
+  op.kind = kind;
+  op.flags = flags;
+  op.K = (int)K;
+  op.nseg = 1;
+  op.nrows = N;
+  op.seg_end[0] = N;
+  op.w[0] = static_cast<const uint8_t*>(W);
+  op.y[0] = y;
+  op.x = x;
+  op.eps = 1e-6f;
+  return op;
+}
+
+int launch_engine(const EngParams& P, int grid, bool cooperative, cudaStream_t s) {
+  cudaError_t e;
+  if (cooperative) {
+    void* args[] = {const_cast<EngParams*>(&P)};
+    e = cudaLaunchCooperativeKernel((const void*)engine_kernel, dim3(grid), dim3(kThreads), args, kSmemAlloc, s);
+  } else {
+    engine_kernel<<<grid, kThreads, kSmemAlloc, s>>>(P);
+    e = cudaGetLastError();
+  }
+  return fak_cuda_status(e);
+}
+
+EngParams base_params() {
+  EngParams P;
+  memset(&P, 0, sizeof(P));
+  P.timeout_ns = 1000000000ull;
+  return P;
+}
+
+int single_matvec(int kind, const void* W, int64_t N, int64_t K, const float* x, float* y, cudaStream_t s) {
+  if (!W || !x || !y) return FAK_ERR_INVALID_ARG;
+  if (N < 1 || N > 0x7fffffffLL || K < 256 || K % 256 != 0 || K > FAK_ENGINE_MAX_K) return FAK_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(x)) return FAK_ERR_ALIGN;
+  int sms = 0;
+  int st = device_setup(&sms);
+  if (st != FAK_OK) return st;
+  EngParams P = base_params();
+  P.inl[0] = make_matvec(kind, W, N, K, x, y, 0);
+  P.n_ops = 1;
+  const int64_t groups = (N + kRowsPerGroup - 1) / kRowsPerGroup;
+  const int grid = (int)std::min<int64_t>(groups, sms);
+  return launch_engine(P, grid, false, s);
+}
+
+}  // namespace
+
+// ================================================================== C ABI
+extern "C" const char* fak_strerror(int status) {
+  switch (status) {
+    case FAK_OK: return "ok";
+    case FAK_ERR_INVALID_ARG: return "invalid argument (null pointer or bad enum)";
+    case FAK_ERR_SHAPE: return "dimension out of the supported range";
+    case FAK_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case FAK_ERR_CUDA: return "CUDA runtime error";
+    case FAK_ERR_TIMEOUT: return "bounded device-side wait timed out";
+    case FAK_ERR_NOMEM: return "device allocation failed";
+    case FAK_ERR_DEVICE: return "device rejected an input (token id out of range)";
+    case FAK_ERR_UNSUPPORTED: return "current device is not sm_103";
+    default: return "unknown status";
+  }
+}
+
+extern "C" const char* fak_version(void) { return "fak-q4k-gb300 0.1 (sm_103a)"; }
+
+extern "C" int fak_q4k_gemv(const void* Wq, int64_t N, int64_t K, const float* x, float* y, fak_stream_t stream) {
+  return single_matvec(OP_Q4K, Wq, N, K, x, y, (cudaStream_t)stream);
+}
+
+extern "C" int fak_q8_0_gemv(const void* Wq, int64_t N, int64_t K, const float* x, float* y, fak_stream_t stream) {
+  return single_matvec(OP_Q8, Wq, N, K, x, y, (cudaStream_t)stream);
+}
+
+extern "C" int fak_q4k_gemv_batch(const void* Wq, int64_t N, int64_t K, const float* X, int M, float* Y,
+                                  fak_stream_t stream) {
+  if (!X || !Y) return FAK_ERR_INVALID_ARG;
+  if (M < 1 || M > 64) return FAK_ERR_SHAPE;
+  for (int m = 0; m < M; ++m) {
+    int st = single_matvec(OP_Q4K, Wq, N, K, X + (int64_t)m * K, Y + (int64_t)m * N, (cudaStream_t)stream);
+    if (st != FAK_OK) return st;
+  }
+  return FAK_OK;
+}
+
+extern "C" int fak_device_status(fak_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return fak_cuda_status(e);
+  int v = 0, zero = 0;
+  e = cudaMemcpyFromSymbol(&v, g_fak_status, sizeof(int));
+  if (e != cudaSuccess) return fak_cuda_status(e);
+  cudaMemcpyToSymbol(g_fak_status, &zero, sizeof(int));
+  return v;
+}
+
+// ------------------------------------------------------------------ MLP decode
+extern "C" size_t fak_mlp_workspace_bytes(int64_t d_ff) {
+  if (d_ff <= 0) return 0;
+  return 256 + (size_t)((d_ff * 4 + 255) / 256 * 256);
+}
+
+extern "C" int fak_mlp_decode(const void* Wgate, const void* Wup, const void* Wdown, int64_t d_model, int64_t d_ff,
+                              const float* x, float eps, float* y, void* workspace, size_t workspace_bytes,
+                              fak_stream_t stream) {
+  if (!Wgate || !Wup || !Wdown || !x || !y || !workspace) return FAK_ERR_INVALID_ARG;
+  if (d_model < 256 || d_model % 256 || d_model > FAK_ENGINE_MAX_K || d_ff < 256 || d_ff % 256 ||
+      d_ff > FAK_ENGINE_MAX_K)
+    return FAK_ERR_SHAPE;
+  if (workspace_bytes < fak_mlp_workspace_bytes(d_ff)) return FAK_ERR_SHAPE;
+  if (!aligned16(Wgate) || !aligned16(Wup) || !aligned16(Wdown) || !aligned16(x) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return FAK_ERR_ALIGN;
+  int sms = 0;
+  int st = device_setup(&sms);
+  if (st != FAK_OK) return st;
+  unsigned* sync = static_cast<unsigned*>(workspace);
+  float* a = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256);
+  EngParams P = base_params();
+  P.inl[0] = make_matvec(OP_Q4K_SWIGLU, Wgate, d_ff, d_model, x, a, F_NORM);
+  P.inl[0].w[1] = static_cast<const uint8_t*>(Wup);
+  P.inl[0].eps = eps;
+  P.inl[1] = make_matvec(OP_Q4K, Wdown, d_model, d_ff, a, y, F_WAIT);
+  P.n_ops = 2;
+  P.sync = sync;
+  cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), (cudaStream_t)stream);
+  if (e != cudaSuccess) return fak_cuda_status(e);
+  return launch_engine(P, sms, true, (cudaStream_t)stream);
+}
+
+// ------------------------------------------------------------------ decode context
+struct fak_decode {
+  fak_decode_desc desc;
+  std::vector<fak_layer_desc> layers;
+  int sms = 0;
+  int mode = 0;
+  int n_ops = 0;
+  int n_fa = 0;
+  EngOp* d_ops = nullptr;
+  std::vector<EngOp> h_ops;
+  float* h = nullptr;
+  float* t = nullptr;
+  float* kv = nullptr;
+  float* a = nullptr;
+  float* cand_val = nullptr;
+  int* cand_idx = nullptr;
+  unsigned* sync = nullptr;
+  int* err = nullptr;
+  unsigned long long timeout_ns = 1000000000ull;
+  int debug_op = -1;
+};
+
+namespace {
+void free_ctx(fak_decode* c) {
+  if (!c) return;
+  cudaFree(c->d_ops);
+  cudaFree(c->h);
+  cudaFree(c->t);
+  cudaFree(c->kv);
+  cudaFree(c->a);
+  cudaFree(c->cand_val);
+  cudaFree(c->cand_idx);
+  cudaFree(c->sync);
+  cudaFree(c->err);
+  delete c;
+}
+
+int upload_ops(fak_decode* c) {
+  std::vector<EngOp> ops = c->h_ops;
+  for (auto& o : ops) o.wait_extra = 0;
+  if (c->debug_op >= 0 && c->debug_op < (int)ops.size()) ops[c->debug_op].wait_extra = 1;
+  return fak_cuda_status(cudaMemcpy(c->d_ops, ops.data(), sizeof(EngOp) * ops.size(), cudaMemcpyHostToDevice));
+}
+}  // namespace
+
+extern "C" int fak_decode_create(const fak_decode_desc* d, fak_decode** out) {
+  if (!d || !out || !d->layers || !d->lm_head || !d->embedding) return FAK_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (d->mode != FAK_DECODE_ONE_LAUNCH && d->mode != FAK_DECODE_PER_MATMUL) return FAK_ERR_INVALID_ARG;
+  auto okdim = [](int64_t v) { return v >= 256 && v % 256 == 0 && v <= FAK_ENGINE_MAX_K; };
+  if (d->n_layers < 0 || !okdim(d->d_model) || !okdim(d->d_ff) || !okdim(d->n_mix) || d->vocab < 1 ||
+      d->gdn_in < 1 || d->fa_qg < 1 || d->fa_kv < 1)
+    return FAK_ERR_SHAPE;
+  int n_fa = 0;
+  for (int l = 0; l < d->n_layers; ++l) {
+    const fak_layer_desc& L = d->layers[l];
+    if (L.kind != FAK_LAYER_GDN && L.kind != FAK_LAYER_FA) return FAK_ERR_INVALID_ARG;
+    if (!L.w_in || !L.w_out || !L.w_gate || !L.w_up || !L.w_down) return FAK_ERR_INVALID_ARG;
+    if (L.kind == FAK_LAYER_FA && (!L.w_k || !L.w_v)) return FAK_ERR_INVALID_ARG;
+    if (d->n_mix > (L.kind == FAK_LAYER_GDN ? d->gdn_in : d->fa_qg)) return FAK_ERR_SHAPE;
+    const void* ps[] = {L.w_in, L.w_k, L.w_v, L.w_out, L.w_gate, L.w_up, L.w_down};
+    for (const void* p : ps)
+      if (p && !aligned16(p)) return FAK_ERR_ALIGN;
+    n_fa += L.kind == FAK_LAYER_FA;
+  }
+  if (!aligned16(d->lm_head) || !aligned16(d->embedding)) return FAK_ERR_ALIGN;
+  int sms = 0;
+  int st = device_setup(&sms);
+  if (st != FAK_OK) return st;
+  fak_decode* c = new fak_decode();
+  c->desc = *d;
+  c->layers.assign(d->layers, d->layers + d->n_layers);
+  c->desc.layers = c->layers.data();
+  c->sms = sms;
+  c->mode = d->mode;
+  c->n_fa = n_fa;
+  if (d->mode == FAK_DECODE_ONE_LAUNCH) {
+    int dev = 0, coop = 0, per_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, engine_kernel, kThreads, kSmemAlloc);
+    if (!coop || per_sm < 1) {
+      delete c;
+      return FAK_ERR_UNSUPPORTED;
+    }
+  }
+  const int64_t D = d->d_model, F = d->d_ff;
+  const int64_t tmax = std::max<int64_t>(d->gdn_in, d->fa_qg);
+  bool okm = cudaMalloc(&c->h, D * 4) == cudaSuccess && cudaMalloc(&c->t, tmax * 4) == cudaSuccess &&
+             cudaMalloc(&c->kv, std::max<int64_t>(1, 2LL * n_fa * d->fa_kv) * 4) == cudaSuccess &&
+             cudaMalloc(&c->a, F * 4) == cudaSuccess && cudaMalloc(&c->cand_val, sms * 4) == cudaSuccess &&
+             cudaMalloc(&c->cand_idx, sms * 4) == cudaSuccess && cudaMalloc(&c->sync, 64) == cudaSuccess &&
+             cudaMalloc(&c->err, 64) == cudaSuccess;
+  if (!okm) {
+    (void)cudaGetLastError();
+    free_ctx(c);
+    return FAK_ERR_NOMEM;
+  }
+  cudaMemset(c->sync, 0, 64);
+  cudaMemset(c->err, 0, 64);
+  cudaMemset(c->kv, 0, std::max<int64_t>(1, 2LL * n_fa * d->fa_kv) * 4);
+
+  // the op list: embed, per layer 4 matvec steps, lm_head + argmax, argmax reduce
+  std::vector<EngOp>& ops = c->h_ops;
+  EngOp e;
+  memset(&e, 0, sizeof(e));
+  e.kind = OP_EMBED;
+  e.K = (int)D;
+  e.vocab = d->vocab;
+  e.x = d->embedding;
+  e.y[0] = c->h;
+  e.nseg = 1;
+  ops.push_back(e);
+  int fa_i = 0;
+  for (int l = 0; l < d->n_layers; ++l) {
+    const fak_layer_desc& L = c->layers[l];
+    EngOp in = make_matvec(OP_Q4K, L.w_in, L.kind == FAK_LAYER_GDN ? d->gdn_in : d->fa_qg, D, c->h, c->t,
+                           F_NORM | F_WAIT);
+    in.eps = d->eps;
+    if (L.kind == FAK_LAYER_FA) {
+      in.nseg = 3;
+      in.seg_end[0] = d->fa_qg;
+      in.seg_end[1] = d->fa_qg + d->fa_kv;
+      in.seg_end[2] = d->fa_qg + 2LL * d->fa_kv;
+      in.nrows = in.seg_end[2];
+      in.w[1] = static_cast<const uint8_t*>(L.w_k);
+      in.w[2] = static_cast<const uint8_t*>(L.w_v);
+      in.y[1] = c->kv + (2LL * fa_i) * d->fa_kv;
+      in.y[2] = c->kv + (2LL * fa_i + 1) * d->fa_kv;
+      ++fa_i;
+    }
+    ops.push_back(in);
+    ops.push_back(make_matvec(OP_Q4K, L.w_out, D, d->n_mix, c->t, c->h, F_RESID | F_WAIT));
+    EngOp gu = make_matvec(OP_Q4K_SWIGLU, L.w_gate, F, D, c->h, c->a, F_NORM | F_WAIT);
+    gu.w[1] = static_cast<const uint8_t*>(L.w_up);
+    gu.eps = d->eps;
+    ops.push_back(gu);
+    ops.push_back(make_matvec(OP_Q4K, L.w_down, D, F, c->a, c->h, F_RESID | F_WAIT));
+  }
+  EngOp lm = make_matvec(OP_Q8, d->lm_head, d->vocab, D, c->h, nullptr, F_NORM | F_WAIT | F_ARGMAX);
+  lm.eps = d->eps;
+  ops.push_back(lm);
+  EngOp am;
+  memset(&am, 0, sizeof(am));
+  am.kind = OP_ARGMAX_REDUCE;
+  am.flags = F_WAIT;
+  am.nseg = 1;
+  ops.push_back(am);
+  c->n_ops = (int)ops.size();
+  if (cudaMalloc(&c->d_ops, sizeof(EngOp) * ops.size()) != cudaSuccess) {
+    (void)cudaGetLastError();
+    free_ctx(c);
+    return FAK_ERR_NOMEM;
+  }
+  st = upload_ops(c);
+  if (st != FAK_OK) {
+    free_ctx(c);
+    return st;
+  }
+  *out = c;
+  return FAK_OK;
+}
+
+extern "C" int fak_decode_step(fak_decode* c, const int32_t* tok_in, int32_t* tok_out, float* logits,
+                               fak_stream_t stream) {
+  if (!c || !tok_in || !tok_out) return FAK_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  EngParams P = base_params();
+  P.ops = c->d_ops;
+  P.err = c->err;
+  P.cand_val = c->cand_val;
+  P.cand_idx = c->cand_idx;
+  P.tok_in = tok_in;
+  P.tok_out = tok_out;
+  P.logits = logits;
+  P.timeout_ns = c->timeout_ns;
+  if (c->mode == FAK_DECODE_ONE_LAUNCH) {
+    P.sync = c->sync;
+    P.n_ops = c->n_ops;
+    P.first_wait = 0;
+    return launch_engine(P, c->sms, true, s);
+  }
+  for (int i = 0; i < c->n_ops; ++i) {
+    P.ops = c->d_ops + i;
+    P.n_ops = 1;
+    P.sync = nullptr;
+    int st = launch_engine(P, c->sms, false, s);
+    if (st != FAK_OK) return st;
+  }
+  return FAK_OK;
+}
+
+extern "C" int fak_decode_status(fak_decode* c, fak_stream_t stream) {
+  if (!c) return FAK_ERR_INVALID_ARG;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return fak_cuda_status(e);
+  int v = 0;
+  e = cudaMemcpy(&v, c->err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fak_cuda_status(e);
+  cudaMemset(c->err, 0, sizeof(int));
+  if (v != 0) cudaMemset(c->sync, 0, 64);
+  return v;
+}
+
+extern "C" int fak_decode_read_state(fak_decode* c, int which, float* dst, size_t count, fak_stream_t stream) {
+  if (!c || !dst || (which != 0 && which != 1)) return FAK_ERR_INVALID_ARG;
+  const size_t n = which == 0 ? (size_t)c->desc.d_model : (size_t)2 * c->n_fa * c->desc.fa_kv;
+  if (count != n) return FAK_ERR_SHAPE;
+  if (n == 0) return FAK_OK;
+  return fak_cuda_status(
+      cudaMemcpyAsync(dst, which == 0 ? c->h : c->kv, n * sizeof(float), cudaMemcpyDefault, (cudaStream_t)stream));
+}
+
+extern "C" int fak_decode_launches_per_step(const fak_decode* c) {
+  if (!c) return 0;
+  return c->mode == FAK_DECODE_ONE_LAUNCH ? 1 : c->n_ops;
+}
+
+extern "C" int fak_decode_set_timeout_ns(fak_decode* c, int64_t ns) {
+  if (!c || ns <= 0) return FAK_ERR_INVALID_ARG;
+  c->timeout_ns = (unsigned long long)ns;
+  return FAK_OK;
+}
+
+extern "C" int fak_decode_debug_unreachable_wait(fak_decode* c, int op_index) {
+  if (!c || op_index >= c->n_ops) return FAK_ERR_INVALID_ARG;
+  c->debug_op = op_index;
+  return upload_ops(c);
+}
+
+extern "C" void fak_decode_destroy(fak_decode* c) { free_ctx(c); }
