@@ -9,12 +9,15 @@
 // where the activation stays on the GPU across every matmul of a token.
 //
 // Design (GB300-first):
-//  * One CTA per SM: 1 producer warp + 8 consumer warps, ~217 KB shared memory.
-//  * The producer streams each CTA's weight rows HBM -> shared memory with
-//    cp.async.bulk into a 16-slot ring (9 KB slots: 8 rows x 8 Q4_K blocks,
-//    or 8 rows x 32 Q8_0 blocks) completing on mbarriers.  It never waits for
-//    activations, so in a multi-step launch it prefetches the next matmul's
-//    weights while the grid waits for the previous step's output.
+//  * One CTA per SM, 8 warps, ~216 KB shared memory.  Each warp owns a double
+//    buffer of 9 KB stages (8 rows x 8 Q4_K blocks, or 8 rows x 32 Q8_0 blocks)
+//    and streams its weight rows HBM -> shared memory with cp.async (16-byte
+//    LDGSTS, L2-only), issuing stage j+1 before computing stage j.  Weights do
+//    not depend on activations, so in a multi-step launch the next matmul's
+//    first stage is already in flight, and the following ones are prefetched
+//    into L2, while the grid waits for the previous step's output.  (Measured
+//    on GB300: per-warp LDGSTS double buffering streams at ~7.2 TB/s, while
+//    1 KB bulk copies from one issuing thread reach only ~0.5 TB/s.)
 //  * Consumers quantize x once per step into shared memory: per 256-element
 //    super-block a power-of-two scale s with |x/s| <= 2^22, X = rint(x/s) split
 //    into three byte limbs (X = X2*65536 + X1*256 + X0, X0/X1 unsigned, X2
@@ -41,9 +44,10 @@
 namespace {
 
 constexpr int kNumConsumerWarps = 8;
-constexpr int kThreads = 32 * (kNumConsumerWarps + 1);
+constexpr int kThreads = 32 * kNumConsumerWarps;
 constexpr int kConsumerThreads = 32 * kNumConsumerWarps;
-constexpr int kStages = 16;
+constexpr int kStages = 2 * kNumConsumerWarps;   // two per warp
+constexpr int kPrefetchStages = 3;               // per warp, into L2, at a step boundary
 constexpr int kStageBytes = 9216;        // 8 rows x 8 Q4_K blocks x 144 B
 constexpr int kRowsPerGroup = 8;
 constexpr int kQ4SlabBlocks = 8;         // Q4_K blocks per row per stage
@@ -136,55 +140,100 @@ __device__ __forceinline__ void set_error(const EngParams& P, int code, volatile
   *abort = 1;
 }
 
-// ------------------------------------------------------------------ producer
-__device__ void producer(const EngParams& P, uint8_t* smem, uint64_t* full, uint64_t* empty, volatile int* abort,
-                         int* issued_out) {
-  const uint64_t pol = l2_evict_first_policy();
-  int q = 0;
-  for (int i = 0; i < P.n_ops && !*abort; ++i) {
-    const EngOp& op = P.ops ? P.ops[i] : P.inl[i];
-    if (!has_weights(op.kind)) continue;
-    const Geo g = geo_of(op);
-    const int64_t ngroups = (op.nrows + g.U - 1) / g.U;
-    int64_t g0, g1;
-    group_range(ngroups, g0, g1);
-    const int64_t row_bytes = (int64_t)g.bpr * g.blk;
-    for (int64_t wv = g0; wv < g1; wv += kNumConsumerWarps) {
-      const int nw = (int)imin64(kNumConsumerWarps, g1 - wv);
-      for (int s = 0; s < g.nslab; ++s) {
-        const int nb = min(g.slab, g.bpr - s * g.slab);
-        const uint32_t bytes_row = (uint32_t)(nb * g.blk);
-        for (int k = 0; k < nw; ++k, ++q) {
-          const int slot = q % kStages;
-          const int use = q / kStages;
-          if (use > 0 && !mbar_wait_bounded(&empty[slot], (use - 1) & 1, abort, P.timeout_ns)) {
-            if (!*abort) set_error(P, FAK_ERR_TIMEOUT, abort);
-            *issued_out = q;
-            return;
-          }
-          const int64_t r0 = (wv + k) * g.U;
-          const int nr = (int)imin64(g.U, op.nrows - r0);
-          uint8_t* stage = smem + kOffRing + slot * kStageBytes;
-          mbar_arrive_expect_tx(&full[slot], bytes_row * nr * (g.pair ? 2 : 1));
-          for (int rl = 0; rl < nr; ++rl) {
-            const int64_t row = r0 + rl;
-            if (g.pair) {
-              const int64_t off = row * row_bytes + (int64_t)s * g.slab * g.blk;
-              bulk_g2s(stage + rl * g.srow, op.w[0] + off, bytes_row, &full[slot], pol);
-              bulk_g2s(stage + (4 + rl) * g.srow, op.w[1] + off, bytes_row, &full[slot], pol);
-            } else {
-              int seg = 0;
-              int64_t seg_start = 0;
-              while (seg < op.nseg - 1 && row >= op.seg_end[seg]) seg_start = op.seg_end[seg++];
-              const uint8_t* src = op.w[seg] + (row - seg_start) * row_bytes + (int64_t)s * g.slab * g.blk;
-              bulk_g2s(stage + rl * g.srow, src, bytes_row, &full[slot], pol);
-            }
-          }
-        }
+// ------------------------------------------------------------------ stage streaming
+// A warp's stages, in order across the steps of the launch: for each step with
+// weights, for each wave of 8 row groups of this CTA, the warp's own group
+// (wave + warp) if it exists, all its slabs.
+struct Cursor {
+  int op;          // step index, n_ops when exhausted
+  int64_t wv;      // wave start group
+  int s;           // slab
+  int64_t g1;      // end group of this CTA for the step
+};
+
+__device__ __forceinline__ bool cursor_settle(const EngParams& P, Cursor& c, int cw) {
+  // move to the first valid stage at or after c
+  while (c.op < P.n_ops) {
+    const EngOp& op = P.ops ? P.ops[c.op] : P.inl[c.op];
+    if (has_weights(op.kind)) {
+      const Geo g = geo_of(op);
+      if (c.wv < 0) {  // entering this step
+        const int64_t ngroups = (op.nrows + g.U - 1) / g.U;
+        int64_t g0;
+        group_range(ngroups, g0, c.g1);
+        c.wv = g0;
+        c.s = 0;
       }
+      while (c.wv < c.g1 && c.wv + cw >= c.g1) c.wv += kNumConsumerWarps;  // no group for this warp
+      if (c.wv < c.g1 && c.s < g.nslab) return true;
     }
+    ++c.op;
+    c.wv = -1;
   }
-  *issued_out = q;
+  return false;
+}
+
+__device__ __forceinline__ void cursor_advance(const EngParams& P, Cursor& c, int cw) {
+  const EngOp& op = P.ops ? P.ops[c.op] : P.inl[c.op];
+  const Geo g = geo_of(op);
+  if (++c.s >= g.nslab) {
+    c.s = 0;
+    c.wv += kNumConsumerWarps;
+  }
+  cursor_settle(P, c, cw);
+}
+
+// Row segment rl (0..7) of a stage: source address and bytes (0 if the row slot is empty).
+__device__ __forceinline__ const uint8_t* stage_row_src(const EngOp& op, const Geo& g, int64_t group, int s, int rl,
+                                                        uint32_t& bytes) {
+  const int64_t row_bytes = (int64_t)g.bpr * g.blk;
+  const int nb = min(g.slab, g.bpr - s * g.slab);
+  const int64_t slab_off = (int64_t)s * g.slab * g.blk;
+  bytes = 0;
+  if (g.pair) {
+    const int64_t row = group * g.U + (rl & 3);
+    if (row >= op.nrows) return nullptr;
+    bytes = (uint32_t)(nb * g.blk);
+    return op.w[rl >> 2] + row * row_bytes + slab_off;
+  }
+  const int64_t row = group * g.U + rl;
+  if (row >= op.nrows) return nullptr;
+  int seg = 0;
+  int64_t seg_start = 0;
+  while (seg < op.nseg - 1 && row >= op.seg_end[seg]) seg_start = op.seg_end[seg++];
+  bytes = (uint32_t)(nb * g.blk);
+  return op.w[seg] + (row - seg_start) * row_bytes + slab_off;
+}
+
+FAK_DEV void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// The whole warp copies one stage into `buf` and commits one cp.async group.
+__device__ void issue_stage(const EngParams& P, const Cursor& c, int cw, int lane, uint8_t* buf) {
+  const EngOp& op = P.ops ? P.ops[c.op] : P.inl[c.op];
+  const Geo g = geo_of(op);
+  const int64_t group = c.wv + cw;
+#pragma unroll 1
+  for (int rl = 0; rl < 8; ++rl) {
+    uint32_t bytes;
+    const uint8_t* src = stage_row_src(op, g, group, c.s, rl, bytes);
+    if (!src) continue;
+    uint8_t* dst = buf + rl * g.srow;
+    for (uint32_t o = (uint32_t)lane * 16; o < bytes; o += 512) cp_async16(dst + o, src + o);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Warm L2 with a stage's rows (one lane per row segment).
+__device__ void prefetch_stage_l2(const EngParams& P, const Cursor& c, int cw, int lane) {
+  if (lane >= 8) return;
+  const EngOp& op = P.ops ? P.ops[c.op] : P.inl[c.op];
+  const Geo g = geo_of(op);
+  uint32_t bytes;
+  const uint8_t* src = stage_row_src(op, g, c.wv + cw, c.s, lane, bytes);
+  if (src && bytes)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // ------------------------------------------------------------------ x preparation
@@ -378,15 +427,31 @@ __device__ __forceinline__ void better(float v, int idx, float& bv, int& bi) {
   }
 }
 
-// ------------------------------------------------------------------ consumers
-__device__ void consumers(const EngParams& P, uint8_t* smem, uint64_t* full, uint64_t* empty, volatile int* abort) {
-  const int ctid = threadIdx.x - 32;
+// ------------------------------------------------------------------ the steps
+__global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_constant__ EngParams P) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  const int ctid = threadIdx.x;
   const int cw = ctid >> 5, lane = ctid & 31;
   float* red = reinterpret_cast<float*>(smem + kOffMisc);          // [8]
   float* bestv = red + 8;                                           // [8]
   int* besti = reinterpret_cast<int*>(red + 16);                    // [8]
-  int q_base = 0;
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 96);
+  if (ctid == 0) *abort = 0;
+  uint8_t* mybuf = smem + kOffRing + (2 * cw) * kStageBytes;
   const unsigned G = gridDim.x;
+
+  // the warp's stream of weight stages, one stage ahead of the compute
+  Cursor ic{0, -1, 0, 0};
+  bool ic_ok = cursor_settle(P, ic, cw);
+  if (ic_ok) {
+    issue_stage(P, ic, cw, lane, mybuf);
+    cursor_advance(P, ic, cw);
+    ic_ok = ic.op < P.n_ops;
+  }
+  int j = 0;  // stages computed by this warp
+  __syncthreads();
+
   for (int i = 0; i < P.n_ops; ++i) {
     const EngOp& op = P.ops ? P.ops[i] : P.inl[i];
     // -- wait for the previous step of this launch to finish on every CTA
@@ -437,73 +502,71 @@ __device__ void consumers(const EngParams& P, uint8_t* smem, uint64_t* full, uin
       group_range(ngroups, g0, g1);
       float wbv = 0.0f;
       int wbi = -1;
-      for (int64_t wv = g0; wv < g1; wv += kNumConsumerWarps) {
-        const int nw = (int)imin64(kNumConsumerWarps, g1 - wv);
-        if (cw < nw && !*abort) {
-          const int64_t r0 = (wv + cw) * g.U;
-          const int nr = (int)imin64(g.U, op.nrows - r0);
-          const uint32_t rowmask = g.pair ? (((1u << nr) - 1) * 0x11u) : ((1u << nr) - 1);
-          float acc[8];
+      for (int64_t wv = g0; wv + cw < g1; wv += kNumConsumerWarps) {
+        const int64_t r0 = (wv + cw) * g.U;
+        const int nr = (int)imin64(g.U, op.nrows - r0);
+        const uint32_t rowmask = g.pair ? (((1u << nr) - 1) * 0x11u) : ((1u << nr) - 1);
+        float acc[8];
 #pragma unroll
-          for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
-          const int qw = q_base + (int)(wv - g0) * g.nslab;
-          for (int s = 0; s < g.nslab; ++s) {
-            const int q = qw + s * nw + cw;
-            const int slot = q % kStages;
-            if (!mbar_wait_bounded(&full[slot], (q / kStages) & 1, abort, P.timeout_ns)) {
-              if (!*abort) set_error(P, FAK_ERR_TIMEOUT, abort);
-              break;
-            }
-            const uint8_t* stage = smem + kOffRing + slot * kStageBytes;
-            const int nb = min(g.slab, g.bpr - s * g.slab);
-            if (g.q8)
-              q8_slab(stage, smem, s * g.slab, nb, rowmask, lane, acc);
-            else
-              q4k_slab(stage, smem, s * g.slab, nb, rowmask, lane, acc);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
+        for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
+        for (int s = 0; s < g.nslab; ++s) {
+          if (ic_ok) {
+            issue_stage(P, ic, cw, lane, mybuf + ((j + 1) & 1) * kStageBytes);
+            cursor_advance(P, ic, cw);
+            ic_ok = ic.op < P.n_ops;
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+          } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
           }
-          // fixed butterfly: every lane ends with the same-order-per-lane totals
+          __syncwarp();
+          const uint8_t* stage = mybuf + (j & 1) * kStageBytes;
+          const int nb = min(g.slab, g.bpr - s * g.slab);
+          if (g.q8)
+            q8_slab(stage, smem, s * g.slab, nb, rowmask, lane, acc);
+          else
+            q4k_slab(stage, smem, s * g.slab, nb, rowmask, lane, acc);
+          __syncwarp();
+          ++j;
+        }
+        // fixed butterfly: every lane ends with the same-order-per-lane totals
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+        }
+        if (g.pair) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            if (lane == r && r < nr) {
+              const float gt = acc[r], up = acc[4 + r];
+              op.y[0][r0 + r] = gt / (1.0f + expf(-gt)) * up;
+            }
+          }
+        } else {
 #pragma unroll
           for (int r = 0; r < 8; ++r) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+            if (lane == r && r < nr) {
+              const int64_t row = r0 + r;
+              int seg = 0;
+              int64_t seg_start = 0;
+              while (seg < op.nseg - 1 && row >= op.seg_end[seg]) seg_start = op.seg_end[seg++];
+              float* yp = op.y[seg] + (row - seg_start);
+              float v = acc[r];
+              if (op.flags & F_RESID) v += ld_cg_f(yp);
+              if (op.flags & F_ARGMAX) {
+                if (P.logits) P.logits[row] = v;
+              } else {
+                *yp = v;
+              }
+            }
           }
-          if (g.pair) {
+          if (op.flags & F_ARGMAX) {
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              if (lane == r && r < nr) {
-                const float gt = acc[r], up = acc[4 + r];
-                op.y[0][r0 + r] = gt / (1.0f + expf(-gt)) * up;
-              }
-            }
-          } else {
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              if (lane == r && r < nr) {
-                const int64_t row = r0 + r;
-                int seg = 0;
-                int64_t seg_start = 0;
-                while (seg < op.nseg - 1 && row >= op.seg_end[seg]) seg_start = op.seg_end[seg++];
-                float* yp = op.y[seg] + (row - seg_start);
-                float v = acc[r];
-                if (op.flags & F_RESID) v += ld_cg_f(yp);
-                if (op.flags & F_ARGMAX) {
-                  if (P.logits) P.logits[row] = v;
-                } else {
-                  *yp = v;
-                }
-              }
-            }
-            if (op.flags & F_ARGMAX) {
-#pragma unroll
-              for (int r = 0; r < 8; ++r)
-                if (r < nr) better(acc[r], (int)(r0 + r), wbv, wbi);
-            }
+            for (int r = 0; r < 8; ++r)
+              if (r < nr) better(acc[r], (int)(r0 + r), wbv, wbi);
           }
         }
       }
-      q_base += (int)(g1 - g0) * g.nslab;
       if (op.flags & F_ARGMAX) {
         if (lane == 0) {
           bestv[cw] = wbv;
@@ -519,6 +582,14 @@ __device__ void consumers(const EngParams& P, uint8_t* smem, uint64_t* full, uin
         }
       }
     }
+    // warm L2 with this warp's next stages while the grid waits at the step boundary
+    if (ic_ok && P.sync) {
+      Cursor pc = ic;
+      for (int k = 0; k < kPrefetchStages && pc.op < P.n_ops; ++k) {
+        prefetch_stage_l2(P, pc, cw, lane);
+        cursor_advance(P, pc, cw);
+      }
+    }
     // -- this CTA finished step i
     named_bar_sync(1, kConsumerThreads);
     if (ctid == 0 && P.sync) {
@@ -526,42 +597,8 @@ __device__ void consumers(const EngParams& P, uint8_t* smem, uint64_t* full, uin
       atomicAdd(&P.sync[0], 1u);
     }
   }
-}
-
-__global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_constant__ EngParams P) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* empty = full + kStages;
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 96);
-  int* issued = reinterpret_cast<int*>(smem + kOffMisc + 100);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    *abort = 0;
-    *issued = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    if (threadIdx.x == 0) {
-      producer(P, smem, full, empty, abort, issued);
-      if (*abort) {
-        // let every copy this CTA issued land before the CTA exits
-        const int q1 = *issued;
-        for (int q = max(0, q1 - kStages); q < q1; ++q) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(&full[q % kStages], (q / kStages) & 1))
-            if (globaltimer_ns() - t0 > 100000000ull) break;
-        }
-      }
-    }
-    __syncwarp();
-  } else {
-    consumers(P, smem, full, empty, abort);
-  }
+  // nothing may still be landing in shared memory when the CTA exits
+  asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
   if (threadIdx.x == 0 && P.sync) {
     __threadfence();
@@ -700,7 +737,8 @@ extern "C" int fak_device_status(fak_stream_t stream) {
   e = cudaMemcpyFromSymbol(&v, g_fak_status, sizeof(int));
   if (e != cudaSuccess) return fak_cuda_status(e);
   cudaMemcpyToSymbol(g_fak_status, &zero, sizeof(int));
-  return v;
+  const int g = fak_gemm_take_status();
+  return v != 0 ? v : g;
 }
 
 // ------------------------------------------------------------------ MLP decode

@@ -141,3 +141,6 @@ static inline int fak_cuda_status(cudaError_t e) {
   (void)cudaGetLastError();
   return FAK_ERR_CUDA;
 }
+
+// Reads and clears the prefill GEMM's device status word (host side, after a sync).
+int fak_gemm_take_status();

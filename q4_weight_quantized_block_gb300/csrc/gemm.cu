@@ -1,30 +1,388 @@
-// Prefill path: SwiGLU between the two prefill GEMMs (the tensor-core GEMM is
-// added in this file next).
+// Prefill dequant-GEMM on the 5th-generation tensor cores (tcgen05 / TMEM),
+// plus the SwiGLU between the two prefill GEMMs.
+//
+// Y[P, N] = X[P, K] * W[N, K]^T with W in Q4_K and X in bf16, f32 accumulate
+// ("Mac Qwen3.6-27B Metal Q4_K perf diagnosis", section 2: mlp_gate_up_proj and
+// mlp_down_proj take 73% of prefill; section 4b: the q4k_gemm prefill kernel).
+//
+// One CTA per SM, persistent over output tiles of 128 weight rows x 256 tokens,
+// K in steps of 64 through a 4-stage shared-memory pipeline:
+//   warp 0      TMA producer: X tile [256 tokens x 64] bf16, 128-byte swizzle
+//   warp 1      TMEM owner + MMA issuer: 4 x tcgen05.mma (M128 N256 K16) per stage
+//   warps 2-5   dequant producers: 128 W rows x 64 weights -> bf16, written in the
+//               same 128-byte-swizzled K-major layout (one thread per row)
+//   warps 6-9   epilogue: tcgen05.ld of the f32 accumulator -> Y (coalesced)
+// Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile overlap
+// the MMAs of the next.  Every wait is bounded; on a timeout the kernel records
+// FAK_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
+#include <mutex>
 
 #include "fak.h"
 #include "fak_device.cuh"
 
 namespace {
+
+constexpr int BM = 128;  // weight rows per tile (MMA M)
+constexpr int BN = 256;  // tokens per tile (MMA N)
+constexpr int BK = 64;   // K per stage (one 128-byte swizzle atom of bf16)
+constexpr int kStagesG = 4;
+constexpr int kThreadsG = 320;
+constexpr int kABytes = BM * BK * 2;  // 16 KB
+constexpr int kBBytes = BN * BK * 2;  // 32 KB
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kStagesG * kABytes;
+constexpr int kOffBarG = kOffB + kStagesG * kBBytes;
+constexpr int kSmemG = kOffBarG + 256;
+constexpr int kSmemAllocG = kSmemG + 1024;
+constexpr uint32_t kTmemCols = 512;
+
+__device__ int g_gemm_status;
+
+FAK_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+FAK_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+FAK_DEV uint64_t sw128_desc(uint32_t smem_addr) {
+  // K-major, 128-byte swizzle: 8-row core groups 1024 bytes apart (SBO), LBO unused (1).
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr >> 4) & 0x3FFF);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for the 5th-generation tensor core
+  d |= (uint64_t)2 << 61;  // SWIZZLE_128B
+  return d;
+}
+
+// kind::f16 instruction descriptor: D f32, A bf16, B bf16, both K-major, N=BN, M=BM.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+FAK_DEV void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+FAK_DEV void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+FAK_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+FAK_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%"
+      "20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct GemmParams {
+  const uint8_t* W;
+  float* Y;
+  int64_t N, K, P;
+  int n_tiles_n, n_tiles_p;
+  unsigned long long timeout_ns;
+};
+
+// Dequantize the 64 weights of one row for K step g (0..3 within a super-block):
+// low nibbles of qs[32g..32g+31] are k 0..31 (sub-block 2g), high nibbles k 32..63
+// (sub-block 2g+1).  w = d*sc*q - dmin*m, rounded once to bf16.
+// `blk` holds the row's 144-byte block as 9 uint4.
+FAK_DEV void dequant_row_step(const uint4 (&blk)[9], int g, uint8_t* row_smem, int r8) {
+  const uint4 h = blk[0];
+  const uint32_t sc_lo = h.y & 0x3F3F3F3Fu, m_lo = h.z & 0x3F3F3F3Fu;
+  const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
+  const uint32_t m_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+  const uint32_t sel = (uint32_t)(2 * g) | ((uint32_t)(2 * g + 1) << 4);
+  const uint32_t scp = prmt(sc_lo, sc_hi, sel), mp = prmt(m_lo, m_hi, sel);
+  const float d = half_bits_to_float(h.x & 0xFFFF), dmin = half_bits_to_float(h.x >> 16);
+  // w = a*q - b = (32a)*(0.5 + q/32) - (16a + b), with 0.5 + q/32 built exactly from the nibble bits
+  float mul[2], add[2];
+#pragma unroll
+  for (int hsel = 0; hsel < 2; ++hsel) {
+    const float a = d * (float)((scp >> (8 * hsel)) & 0xFF);
+    const float b = dmin * (float)((mp >> (8 * hsel)) & 0xFF);
+    mul[hsel] = 32.0f * a;
+    add[hsel] = -(16.0f * a + b);
+  }
+  const uint4 q0 = blk[1 + 2 * g], q1 = blk[2 + 2 * g];
+  const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+  for (int hsel = 0; hsel < 2; ++hsel) {
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {  // 16-byte chunk (8 weights) c = 4*hsel + c4
+      uint32_t packed[4];
+#pragma unroll
+      for (int wi = 0; wi < 2; ++wi) {
+        const uint32_t wsrc = qw[2 * c4 + wi];
+        const uint32_t t = hsel == 0 ? ((wsrc << 3) & 0x78787878u) : ((wsrc >> 1) & 0x78787878u);
+        float f[4];
+#pragma unroll
+        for (int bi = 0; bi < 4; ++bi) {
+          const uint32_t bits = prmt(t, 0x3F000000u, 0x7044u | ((uint32_t)bi << 8));
+          f[bi] = fmaf(mul[hsel], __uint_as_float(bits), add[hsel]);
+        }
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(f[0], f[1]);
+        __nv_bfloat162 p1 = __floats2bfloat162_rn(f[2], f[3]);
+        packed[2 * wi] = *reinterpret_cast<uint32_t*>(&p0);
+        packed[2 * wi + 1] = *reinterpret_cast<uint32_t*>(&p1);
+      }
+      const int c = 4 * hsel + c4;
+      *reinterpret_cast<uint4*>(row_smem + ((c ^ r8) << 4)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreadsG, 1)
+    q4k_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ GemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_x = reinterpret_cast<uint64_t*>(smem + kOffBarG);
+  uint64_t* full_w = full_x + kStagesG;
+  uint64_t* empty = full_w + kStagesG;
+  uint64_t* tfull = empty + kStagesG;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesG; ++s) {
+      mbar_init(&full_x[s], 1);
+      mbar_init(&full_w[s], 4);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int ktiles = (int)(p.K / BK);
+  const int total_tiles = p.n_tiles_n * p.n_tiles_p;
+  const uint64_t tmo = p.timeout_ns;
+  auto fail = [&]() {
+    atomicCAS(&g_gemm_status, 0, FAK_ERR_TIMEOUT);
+    *abort = 1;
+  };
+
+  if (warp == 0) {
+    // ---------------- TMA producer (X)
+    if (lane == 0) {
+      int it = 0;
+      for (int tile = blockIdx.x; tile < total_tiles && !*abort; tile += gridDim.x) {
+        const int p0 = (tile % p.n_tiles_p) * BN;
+        for (int kt = 0; kt < ktiles; ++kt, ++it) {
+          const int s = it % kStagesG;
+          if (it >= kStagesG && !mbar_wait_bounded(&empty[s], ((it / kStagesG) - 1) & 1, abort, tmo)) {
+            if (!*abort) fail();
+            break;
+          }
+          mbar_arrive_expect_tx(&full_x[s], kBBytes);
+          tma_load_2d(smem + kOffB + s * kBBytes, &xmap, kt * BK, p0, &full_x[s]);
+        }
+      }
+      // let in-flight copies land before the CTA can exit
+      const int last = it;
+      for (int q = last - kStagesG < 0 ? 0 : last - kStagesG; q < last; ++q) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&full_x[q % kStagesG], (q / kStagesG) & 1))
+          if (globaltimer_ns() - t0 > 200000000ull) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      int it = 0, local = 0;
+      for (int tile = blockIdx.x; tile < total_tiles && !*abort; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        if (local >= 2 && !mbar_wait_bounded(&tempty[acc], ((local >> 1) - 1) & 1, abort, tmo)) {
+          if (!*abort) fail();
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dcol = tmem + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kt = 0; kt < ktiles; ++kt, ++it) {
+          const int s = it % kStagesG;
+          const uint32_t ph = (it / kStagesG) & 1;
+          if (!mbar_wait_bounded(&full_x[s], ph, abort, tmo) || !mbar_wait_bounded(&full_w[s], ph, abort, tmo)) {
+            if (!*abort) fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_desc(smem_u32(smem + kOffA + s * kABytes));
+          const uint64_t bd = sw128_desc(smem_u32(smem + kOffB + s * kBBytes));
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16(dcol, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), (kt | kk) != 0);
+          mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+      }
+      // all issued MMAs complete before TMEM can be freed
+      mma_commit(drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(drain, 0))
+        if (globaltimer_ns() - t0 > 200000000ull) break;
+    }
+  } else if (warp < 6) {
+    // ---------------- dequant producers: thread t owns row t of each W tile
+    const int t = threadIdx.x - 64;
+    const int r8 = t & 7;
+    const int64_t row_bytes = p.K / 256 * 144;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total_tiles && !*abort; tile += gridDim.x) {
+      const int64_t n = (int64_t)(tile / p.n_tiles_p) * BM + t;
+      const uint4* src = reinterpret_cast<const uint4*>(p.W + n * row_bytes);
+      uint4 blk[9], nxt[9];
+#pragma unroll
+      for (int i = 0; i < 9; ++i) nxt[i] = __ldg(src + i);
+      bool ok = true;
+      for (int kt = 0; kt < ktiles && ok; ++kt, ++it) {
+        const int g = kt & 3;
+        if (g == 0) {
+#pragma unroll
+          for (int i = 0; i < 9; ++i) blk[i] = nxt[i];
+          if (kt + 4 < ktiles) {
+            const uint4* s2 = src + (kt / 4 + 1) * 9;
+#pragma unroll
+            for (int i = 0; i < 9; ++i) nxt[i] = __ldg(s2 + i);
+          }
+        }
+        const int s = it % kStagesG;
+        if (it >= kStagesG && !mbar_wait_bounded(&empty[s], ((it / kStagesG) - 1) & 1, abort, tmo)) {
+          if (!*abort) fail();
+          ok = false;
+          break;
+        }
+        uint8_t* row_smem = smem + kOffA + s * kABytes + (t >> 3) * 1024 + r8 * 128;
+        dequant_row_step(blk, g, row_smem, r8);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full_w[s]);
+      }
+      if (!ok) break;
+    }
+  } else {
+    // ---------------- epilogue: TMEM lanes 32*(warp%4) .. +31
+    const int q = warp & 3;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total_tiles && !*abort; tile += gridDim.x, ++local) {
+      const int acc = local & 1;
+      if (!mbar_wait_bounded(&tfull[acc], (local >> 1) & 1, abort, tmo)) {
+        if (!*abort) fail();
+        break;
+      }
+      tc_fence_after();
+      const int64_t n = (int64_t)(tile / p.n_tiles_p) * BM + 32 * q + lane;
+      const int64_t p0 = (int64_t)(tile % p.n_tiles_p) * BN;
+#pragma unroll 1
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN + 32 * ch), r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int64_t pp = p0 + 32 * ch + j;
+          if (pp < p.P) p.Y[pp * p.N + n] = __uint_as_float(r[j]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
 __global__ void swiglu_bf16_kernel(const float* __restrict__ Y1, int64_t P, int64_t half,
                                    __nv_bfloat16* __restrict__ X2) {
   const int64_t total = P * half;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t p = i / half, c = i - p * half;
-    const float g = Y1[p * 2 * half + c], u = Y1[p * 2 * half + half + c];
+    const int64_t r = i / half, c = i - r * half;
+    const float g = Y1[r * 2 * half + c], u = Y1[r * 2 * half + half + c];
     X2[i] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * u);
   }
 }
+
+std::mutex g_gemm_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_gemm_attr[64] = {};
+
+int gemm_setup(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fak_cuda_status(e);
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) return FAK_ERR_UNSUPPORTED;
+  cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  std::lock_guard<std::mutex> lk(g_gemm_mu);
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return fak_cuda_status(e);
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (dev >= 0 && dev < 64 && !g_gemm_attr[dev]) {
+    e = cudaFuncSetAttribute(q4k_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAllocG);
+    if (e != cudaSuccess) return fak_cuda_status(e);
+    g_gemm_attr[dev] = true;
+  }
+  return FAK_OK;
+}
+
 }  // namespace
 
 extern "C" int fak_swiglu_bf16(const float* Y1, int64_t P, int64_t half, void* X2, fak_stream_t stream) {
   if (!Y1 || !X2) return FAK_ERR_INVALID_ARG;
   if (P < 1 || half < 1) return FAK_ERR_SHAPE;
   const int64_t total = P * half;
-  const int grid = (int)((total + 255) / 256 < 152 * 16 ? (total + 255) / 256 : 152 * 16);
+  const int64_t want = (total + 255) / 256;
+  const int grid = (int)(want < 152 * 16 ? want : 152 * 16);
   swiglu_bf16_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(Y1, P, half, static_cast<__nv_bfloat16*>(X2));
   return fak_cuda_status(cudaGetLastError());
 }
@@ -32,7 +390,42 @@ extern "C" int fak_swiglu_bf16(const float* Y1, int64_t P, int64_t half, void* X
 extern "C" int fak_q4k_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, float* Y,
                             fak_stream_t stream) {
   if (!Wq || !X || !Y) return FAK_ERR_INVALID_ARG;
-  if (K < 256 || K % 256 || N < 128 || N % 128 || P < 1) return FAK_ERR_SHAPE;
-  (void)stream;
-  return FAK_ERR_UNSUPPORTED;
+  if (K < 256 || K % 256 || N < 128 || N % 128 || P < 1 || P > (1LL << 31) - 1 || K > (1LL << 31) - 1)
+    return FAK_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(Wq) & 15) || (reinterpret_cast<uintptr_t>(X) & 15)) return FAK_ERR_ALIGN;
+  int sms = 0;
+  int st = gemm_setup(&sms);
+  if (st != FAK_OK) return st;
+  CUtensorMap map;
+  memset(&map, 0, sizeof(map));
+  const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)P};
+  const cuuint64_t gstride[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {BK, BN};
+  const cuuint32_t estride[2] = {1, 1};
+  CUresult r = g_encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), gdim, gstride, box, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return FAK_ERR_CUDA;
+  GemmParams gp;
+  gp.W = static_cast<const uint8_t*>(Wq);
+  gp.Y = Y;
+  gp.N = N;
+  gp.K = K;
+  gp.P = P;
+  gp.n_tiles_n = (int)(N / BM);
+  gp.n_tiles_p = (int)((P + BN - 1) / BN);
+  gp.timeout_ns = 2000000000ull;
+  const int tiles = gp.n_tiles_n * gp.n_tiles_p;
+  const int grid = tiles < sms ? tiles : sms;
+  q4k_gemm_kernel<<<grid, kThreadsG, kSmemAllocG, (cudaStream_t)stream>>>(map, gp);
+  return fak_cuda_status(cudaGetLastError());
+}
+
+int fak_gemm_take_status() {
+  int v = 0, zero = 0;
+  cudaError_t e;
+  e = cudaMemcpyFromSymbol(&v, g_gemm_status, sizeof(int));
+  if (e != cudaSuccess) return fak_cuda_status(e);
+  cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof(int));
+  return v;
 }
