@@ -118,7 +118,7 @@ __device__ __forceinline__ Geo geo_of(const EngOp& op) {
   g.U = g.pair ? 4 : kRowsPerGroup;
   g.bpr = g.q8 ? op.K / 32 : op.K / 256;
   g.slab = g.q8 ? kQ8SlabBlocks : kQ4SlabBlocks;
-  g.nslab = (g.bpr + g.slab - 1) / g.slab;
+  g.nslab = g.q8 ? (g.bpr + kQ8SlabBlocks - 1) / kQ8SlabBlocks : (g.bpr + kQ4SlabBlocks - 1) / kQ4SlabBlocks;
   g.blk = g.q8 ? 34 : 144;
   g.srow = g.q8 ? kQ8StageRow : kQ4StageRow;
   return g;
@@ -128,10 +128,21 @@ __device__ __forceinline__ bool has_weights(int kind) {
   return kind == OP_Q4K || kind == OP_Q4K_SWIGLU || kind == OP_Q8;
 }
 
-__device__ __forceinline__ void group_range(int64_t ngroups, int64_t& g0, int64_t& g1) {
-  const int64_t c = blockIdx.x, G = gridDim.x;
-  g0 = ngroups * c / G;
-  g1 = ngroups * (c + 1) / G;
+// Every warp of the grid owns a contiguous range of output rows of a step
+// (balanced to one row), processed as groups of U rows.
+struct Plan {
+  int64_t r_lo, r_hi;
+  int ngroups;
+};
+
+__device__ __forceinline__ Plan plan_of(const EngOp& op, const Geo& g, int cw) {
+  const int64_t GW = (int64_t)gridDim.x * kNumConsumerWarps;
+  const int64_t gw = (int64_t)blockIdx.x * kNumConsumerWarps + cw;
+  Plan p;
+  p.r_lo = op.nrows * gw / GW;
+  p.r_hi = op.nrows * (gw + 1) / GW;
+  p.ngroups = (int)((p.r_hi - p.r_lo + g.U - 1) / g.U);
+  return p;
 }
 
 __device__ __forceinline__ void set_error(const EngParams& P, int code, volatile int* abort) {
@@ -142,98 +153,97 @@ __device__ __forceinline__ void set_error(const EngParams& P, int code, volatile
 
 // ------------------------------------------------------------------ stage streaming
 // A warp's stages, in order across the steps of the launch: for each step with
-// weights, for each wave of 8 row groups of this CTA, the warp's own group
-// (wave + warp) if it exists, all its slabs.
+// weights, for each of the warp's row groups, all slabs.
 struct Cursor {
   int op;          // step index, n_ops when exhausted
-  int64_t wv;      // wave start group
+  int grp;         // group within the warp's rows
   int s;           // slab
-  int64_t g1;      // end group of this CTA for the step
+  int ngroups, nslab;
+  int64_t r_lo, r_hi;
 };
 
+__device__ __forceinline__ void cursor_load(const EngParams& P, Cursor& c, int cw) {
+  c.grp = 0;
+  c.s = 0;
+  c.ngroups = 0;
+  if (c.op >= P.n_ops) return;
+  const EngOp& op = P.ops ? P.ops[c.op] : P.inl[c.op];
+  if (!has_weights(op.kind)) return;
+  const Geo g = geo_of(op);
+  const Plan pl = plan_of(op, g, cw);
+  c.ngroups = pl.ngroups;
+  c.nslab = g.nslab;
+  c.r_lo = pl.r_lo;
+  c.r_hi = pl.r_hi;
+}
+
 __device__ __forceinline__ bool cursor_settle(const EngParams& P, Cursor& c, int cw) {
-  // move to the first valid stage at or after c
-  while (c.op < P.n_ops) {
-    const EngOp& op = P.ops ? P.ops[c.op] : P.inl[c.op];
-    if (has_weights(op.kind)) {
-      const Geo g = geo_of(op);
-      if (c.wv < 0) {  // entering this step
-        const int64_t ngroups = (op.nrows + g.U - 1) / g.U;
-        int64_t g0;
-        group_range(ngroups, g0, c.g1);
-        c.wv = g0;
-        c.s = 0;
-      }
-      while (c.wv < c.g1 && c.wv + cw >= c.g1) c.wv += kNumConsumerWarps;  // no group for this warp
-      if (c.wv < c.g1 && c.s < g.nslab) return true;
-    }
+  while (c.op < P.n_ops && c.grp >= c.ngroups) {
     ++c.op;
-    c.wv = -1;
+    cursor_load(P, c, cw);
   }
-  return false;
+  return c.op < P.n_ops;
 }
 
 __device__ __forceinline__ void cursor_advance(const EngParams& P, Cursor& c, int cw) {
-  const EngOp& op = P.ops ? P.ops[c.op] : P.inl[c.op];
-  const Geo g = geo_of(op);
-  if (++c.s >= g.nslab) {
+  if (++c.s >= c.nslab) {
     c.s = 0;
-    c.wv += kNumConsumerWarps;
+    ++c.grp;
   }
   cursor_settle(P, c, cw);
 }
 
-// Row segment rl (0..7) of a stage: source address and bytes (0 if the row slot is empty).
-__device__ __forceinline__ const uint8_t* stage_row_src(const EngOp& op, const Geo& g, int64_t group, int s, int rl,
-                                                        uint32_t& bytes) {
-  const int64_t row_bytes = (int64_t)g.bpr * g.blk;
-  const int nb = min(g.slab, g.bpr - s * g.slab);
-  const int64_t slab_off = (int64_t)s * g.slab * g.blk;
-  bytes = 0;
-  if (g.pair) {
-    const int64_t row = group * g.U + (rl & 3);
-    if (row >= op.nrows) return nullptr;
-    bytes = (uint32_t)(nb * g.blk);
-    return op.w[rl >> 2] + row * row_bytes + slab_off;
-  }
-  const int64_t row = group * g.U + rl;
-  if (row >= op.nrows) return nullptr;
+// Source of output row `row` (segment lookup) at slab offset 0.
+__device__ __forceinline__ const uint8_t* row_src(const EngOp& op, int64_t row, int64_t row_bytes) {
   int seg = 0;
   int64_t seg_start = 0;
   while (seg < op.nseg - 1 && row >= op.seg_end[seg]) seg_start = op.seg_end[seg++];
-  bytes = (uint32_t)(nb * g.blk);
-  return op.w[seg] + (row - seg_start) * row_bytes + slab_off;
+  return op.w[seg] + (row - seg_start) * row_bytes;
 }
 
 FAK_DEV void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
+// Stage row slot rl: source (or NULL if empty) for the cursor's group and slab.
+__device__ __forceinline__ const uint8_t* slot_src(const EngOp& op, const Geo& g, const Cursor& c, int rl) {
+  const int64_t row_bytes = (int64_t)g.bpr * g.blk;
+  const int64_t off = (int64_t)c.s * g.slab * g.blk;
+  const int64_t row0 = c.r_lo + (int64_t)c.grp * g.U;
+  if (g.pair) {
+    const int64_t row = row0 + (rl & 3);
+    if (row >= c.r_hi) return nullptr;
+    return op.w[rl >> 2] + row * row_bytes + off;
+  }
+  const int64_t row = row0 + rl;
+  if (row >= c.r_hi) return nullptr;
+  return row_src(op, row, row_bytes) + off;
+}
+
 // The whole warp copies one stage into `buf` and commits one cp.async group.
-__device__ void issue_stage(const EngParams& P, const Cursor& c, int cw, int lane, uint8_t* buf) {
+__device__ void issue_stage(const EngParams& P, const Cursor& c, int lane, uint8_t* buf) {
   const EngOp& op = P.ops ? P.ops[c.op] : P.inl[c.op];
   const Geo g = geo_of(op);
-  const int64_t group = c.wv + cw;
+  const int nb = min(g.slab, g.bpr - c.s * g.slab);
+  const int nch = nb * g.blk / 16;
 #pragma unroll 1
   for (int rl = 0; rl < 8; ++rl) {
-    uint32_t bytes;
-    const uint8_t* src = stage_row_src(op, g, group, c.s, rl, bytes);
+    const uint8_t* src = slot_src(op, g, c, rl);
     if (!src) continue;
     uint8_t* dst = buf + rl * g.srow;
-    for (uint32_t o = (uint32_t)lane * 16; o < bytes; o += 512) cp_async16(dst + o, src + o);
+    for (int ch = lane; ch < nch; ch += 32) cp_async16(dst + 16 * ch, src + 16 * ch);
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-// Warm L2 with a stage's rows (one lane per row segment).
-__device__ void prefetch_stage_l2(const EngParams& P, const Cursor& c, int cw, int lane) {
+// Warm L2 with a stage's rows (one lane per row slot).
+__device__ void prefetch_stage_l2(const EngParams& P, const Cursor& c, int lane) {
   if (lane >= 8) return;
   const EngOp& op = P.ops ? P.ops[c.op] : P.inl[c.op];
   const Geo g = geo_of(op);
-  uint32_t bytes;
-  const uint8_t* src = stage_row_src(op, g, c.wv + cw, c.s, lane, bytes);
-  if (src && bytes)
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+  const uint8_t* src = slot_src(op, g, c, lane);
+  const int nb = min(g.slab, g.bpr - c.s * g.slab);
+  if (src) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"((uint32_t)(nb * g.blk)) : "memory");
 }
 
 // ------------------------------------------------------------------ x preparation
@@ -310,9 +320,50 @@ __device__ void prepare_x(const EngOp& op, uint8_t* smem, float* red, int cw, in
 }
 
 // ------------------------------------------------------------------ Q4_K slab
-// One stage: up to 8 rows x up to 8 blocks.  Lane (b, g) = (lane/4, lane%4)
+// One stage: up to 8 row slots x up to 8 blocks.  Lane (b, g) = (lane/4, lane%4)
 // covers block b of the slab and its 64-weight group g (sub-blocks 2g, 2g+1).
-__device__ __forceinline__ void q4k_slab(const uint8_t* stage, const uint8_t* smem, int jb0, int nb, uint32_t rowmask,
+// Row slots are computed in pairs without branches (slots past the valid rows
+// hold stale bytes; their sums are never written).
+struct XRegs {
+  uint32_t A0[8], A1[8], A2[8], B0[8], B1[8], B2[8];
+  float SA, SB, sx16;
+};
+
+__device__ __forceinline__ float q4k_row(const uint8_t* base, const XRegs& x, int g, uint32_t sel, float acc) {
+  const uint4 h = *reinterpret_cast<const uint4*>(base);
+  const uint4 qa = *reinterpret_cast<const uint4*>(base + 16 + 32 * g);
+  const uint4 qb = *reinterpret_cast<const uint4*>(base + 32 + 32 * g);
+  const uint32_t sc_lo = h.y & 0x3F3F3F3Fu;
+  const uint32_t m_lo = h.z & 0x3F3F3F3Fu;
+  const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
+  const uint32_t m_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+  const uint32_t scp = prmt(sc_lo, sc_hi, sel);
+  const uint32_t mp = prmt(m_lo, m_hi, sel);
+  const int scA16 = (int)(scp & 0xFF) << 4, scB = (int)((scp >> 8) & 0xFF);
+  const float mA = (float)(mp & 0xFF), mB = (float)((mp >> 8) & 0xFF);
+  const float d = half_bits_to_float(h.x & 0xFFFF), dmin = half_bits_to_float(h.x >> 16);
+  const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+  uint32_t a0 = 0, a1 = 0, b0 = 0, b1 = 0;
+  int a2 = 0, b2 = 0;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint32_t lo = w[u] & 0x0F0F0F0Fu, hi = w[u] & 0xF0F0F0F0u;
+    a0 = dp4a_uu(lo, x.A0[u], a0);
+    a1 = dp4a_uu(lo, x.A1[u], a1);
+    a2 = dp4a_us(lo, x.A2[u], a2);
+    b0 = dp4a_uu(hi, x.B0[u], b0);
+    b1 = dp4a_uu(hi, x.B1[u], b1);
+    b2 = dp4a_us(hi, x.B2[u], b2);
+  }
+  const int J0 = (int)a0 * scA16 + (int)b0 * scB;
+  const int J1 = (int)a1 * scA16 + (int)b1 * scB;
+  const int J2 = a2 * scA16 + b2 * scB;
+  const float Jf = fmaf((float)J2, 65536.0f, fmaf((float)J1, 256.0f, (float)J0));
+  const float mterm = fmaf(mA, x.SA, mB * x.SB);
+  return fmaf(d * x.sx16, Jf, fmaf(-dmin, mterm, acc));
+}
+
+__device__ __forceinline__ void q4k_slab(const uint8_t* stage, const uint8_t* smem, int jb0, int nb, int nslots,
                                          int lane, float acc[8]) {
   const int b = lane >> 2, g = lane & 3;
   if (b >= nb) return;
@@ -320,102 +371,74 @@ __device__ __forceinline__ void q4k_slab(const uint8_t* stage, const uint8_t* sm
   const uint8_t* rec = smem + kOffX + jb * kSuperBytes + (2 * g) * kRecBytes;
   const uint4* r0 = reinterpret_cast<const uint4*>(rec);
   const uint4* r1 = reinterpret_cast<const uint4*>(rec + kRecBytes);
-  uint32_t A0w[8], A1w[8], A2w[8], B0w[8], B1w[8], B2w[8];
-  {
+  XRegs x;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
     uint4 t;
-    t = r0[0]; A0w[0] = t.x; A0w[1] = t.y; A0w[2] = t.z; A0w[3] = t.w;
-    t = r0[1]; A0w[4] = t.x; A0w[5] = t.y; A0w[6] = t.z; A0w[7] = t.w;
-    t = r0[2]; A1w[0] = t.x; A1w[1] = t.y; A1w[2] = t.z; A1w[3] = t.w;
-    t = r0[3]; A1w[4] = t.x; A1w[5] = t.y; A1w[6] = t.z; A1w[7] = t.w;
-    t = r0[4]; A2w[0] = t.x; A2w[1] = t.y; A2w[2] = t.z; A2w[3] = t.w;
-    t = r0[5]; A2w[4] = t.x; A2w[5] = t.y; A2w[6] = t.z; A2w[7] = t.w;
-    t = r1[0]; B0w[0] = t.x; B0w[1] = t.y; B0w[2] = t.z; B0w[3] = t.w;
-    t = r1[1]; B0w[4] = t.x; B0w[5] = t.y; B0w[6] = t.z; B0w[7] = t.w;
-    t = r1[2]; B1w[0] = t.x; B1w[1] = t.y; B1w[2] = t.z; B1w[3] = t.w;
-    t = r1[3]; B1w[4] = t.x; B1w[5] = t.y; B1w[6] = t.z; B1w[7] = t.w;
-    t = r1[4]; B2w[0] = t.x; B2w[1] = t.y; B2w[2] = t.z; B2w[3] = t.w;
-    t = r1[5]; B2w[4] = t.x; B2w[5] = t.y; B2w[6] = t.z; B2w[7] = t.w;
+    t = r0[0 + h]; x.A0[4 * h] = t.x; x.A0[4 * h + 1] = t.y; x.A0[4 * h + 2] = t.z; x.A0[4 * h + 3] = t.w;
+    t = r0[2 + h]; x.A1[4 * h] = t.x; x.A1[4 * h + 1] = t.y; x.A1[4 * h + 2] = t.z; x.A1[4 * h + 3] = t.w;
+    t = r0[4 + h]; x.A2[4 * h] = t.x; x.A2[4 * h + 1] = t.y; x.A2[4 * h + 2] = t.z; x.A2[4 * h + 3] = t.w;
+    t = r1[0 + h]; x.B0[4 * h] = t.x; x.B0[4 * h + 1] = t.y; x.B0[4 * h + 2] = t.z; x.B0[4 * h + 3] = t.w;
+    t = r1[2 + h]; x.B1[4 * h] = t.x; x.B1[4 * h + 1] = t.y; x.B1[4 * h + 2] = t.z; x.B1[4 * h + 3] = t.w;
+    t = r1[4 + h]; x.B2[4 * h] = t.x; x.B2[4 * h + 1] = t.y; x.B2[4 * h + 2] = t.z; x.B2[4 * h + 3] = t.w;
   }
   const float* xS = reinterpret_cast<const float*>(smem + kOffS);
-  const float SA = xS[jb * 8 + 2 * g], SB = xS[jb * 8 + 2 * g + 1];
-  const float sx16 = reinterpret_cast<const float*>(smem + kOffScale)[jb] * 0.0625f;
+  x.SA = xS[jb * 8 + 2 * g];
+  x.SB = xS[jb * 8 + 2 * g + 1];
+  x.sx16 = reinterpret_cast<const float*>(smem + kOffScale)[jb] * 0.0625f;
   const uint32_t sel = (uint32_t)(2 * g) | ((uint32_t)(2 * g + 1) << 4);
+  const uint8_t* base = stage + b * 144;
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    if (!((rowmask >> r) & 1)) continue;
-    const uint8_t* base = stage + r * kQ4StageRow + b * 144;
-    const uint4 h = *reinterpret_cast<const uint4*>(base);
-    const uint4 qa = *reinterpret_cast<const uint4*>(base + 16 + 32 * g);
-    const uint4 qb = *reinterpret_cast<const uint4*>(base + 32 + 32 * g);
-    const uint32_t sc_lo = h.y & 0x3F3F3F3Fu;
-    const uint32_t m_lo = h.z & 0x3F3F3F3Fu;
-    const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
-    const uint32_t m_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
-    const uint32_t scp = prmt(sc_lo, sc_hi, sel);
-    const uint32_t mp = prmt(m_lo, m_hi, sel);
-    const int scA16 = (int)(scp & 0xFF) << 4, scB = (int)((scp >> 8) & 0xFF);
-    const float mA = (float)(mp & 0xFF), mB = (float)((mp >> 8) & 0xFF);
-    const float d = half_bits_to_float(h.x & 0xFFFF), dmin = half_bits_to_float(h.x >> 16);
-    const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-    uint32_t a0 = 0, a1 = 0, b0 = 0, b1 = 0;
-    int a2 = 0, b2 = 0;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const uint32_t lo = w[u] & 0x0F0F0F0Fu, hi = w[u] & 0xF0F0F0F0u;
-      a0 = dp4a_uu(lo, A0w[u], a0);
-      a1 = dp4a_uu(lo, A1w[u], a1);
-      a2 = dp4a_us(lo, A2w[u], a2);
-      b0 = dp4a_uu(hi, B0w[u], b0);
-      b1 = dp4a_uu(hi, B1w[u], b1);
-      b2 = dp4a_us(hi, B2w[u], b2);
-    }
-    const int J0 = (int)a0 * scA16 + (int)b0 * scB;
-    const int J1 = (int)a1 * scA16 + (int)b1 * scB;
-    const int J2 = a2 * scA16 + b2 * scB;
-    const float Jf = fmaf((float)J2, 65536.0f, fmaf((float)J1, 256.0f, (float)J0));
-    const float mterm = fmaf(mA, SA, mB * SB);
-    acc[r] = fmaf(d * sx16, Jf, fmaf(-dmin, mterm, acc[r]));
+  for (int rp = 0; rp < 4; ++rp) {
+    if (2 * rp >= nslots) break;
+    acc[2 * rp] = q4k_row(base + (2 * rp) * kQ4StageRow, x, g, sel, acc[2 * rp]);
+    acc[2 * rp + 1] = q4k_row(base + (2 * rp + 1) * kQ4StageRow, x, g, sel, acc[2 * rp + 1]);
   }
 }
 
 // ------------------------------------------------------------------ Q8_0 slab
-// One stage: up to 8 rows x up to 32 blocks; lane l covers block l.
-__device__ __forceinline__ void q8_slab(const uint8_t* stage, const uint8_t* smem, int cb0, int nb, uint32_t rowmask,
+// One stage: up to 8 row slots x up to 32 blocks; lane l covers block l.
+__device__ __forceinline__ float q8_row(const uint8_t* rowbase, int lane, const uint32_t (&P0)[8],
+                                        const uint32_t (&P1)[8], const uint32_t (&P2)[8], float sx, uint32_t sel,
+                                        int odd, float acc) {
+  const uint32_t* wp = reinterpret_cast<const uint32_t*>(rowbase + ((34 * lane) & ~3));
+  uint32_t w[9];
+#pragma unroll
+  for (int u = 0; u < 9; ++u) w[u] = wp[u];
+  const float d = half_bits_to_float(odd ? (w[0] >> 16) : (w[0] & 0xFFFF));
+  int i0 = 0, i1 = 0, i2 = 0;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint32_t q = prmt(w[u], w[u + 1], sel);
+    i0 = dp4a_su(q, P0[u], i0);
+    i1 = dp4a_su(q, P1[u], i1);
+    i2 = dp4a_ss(q, P2[u], i2);
+  }
+  const float Jf = fmaf((float)i2, 65536.0f, fmaf((float)i1, 256.0f, (float)i0));
+  return fmaf(d * sx, Jf, acc);
+}
+
+__device__ __forceinline__ void q8_slab(const uint8_t* stage, const uint8_t* smem, int cb0, int nb, int nslots,
                                         int lane, float acc[8]) {
   if (lane >= nb) return;
   const int cb = cb0 + lane;
   const uint4* rec = reinterpret_cast<const uint4*>(smem + kOffX + (cb >> 3) * kSuperBytes + (cb & 7) * kRecBytes);
   uint32_t P0[8], P1[8], P2[8];
-  {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
     uint4 t;
-    t = rec[0]; P0[0] = t.x; P0[1] = t.y; P0[2] = t.z; P0[3] = t.w;
-    t = rec[1]; P0[4] = t.x; P0[5] = t.y; P0[6] = t.z; P0[7] = t.w;
-    t = rec[2]; P1[0] = t.x; P1[1] = t.y; P1[2] = t.z; P1[3] = t.w;
-    t = rec[3]; P1[4] = t.x; P1[5] = t.y; P1[6] = t.z; P1[7] = t.w;
-    t = rec[4]; P2[0] = t.x; P2[1] = t.y; P2[2] = t.z; P2[3] = t.w;
-    t = rec[5]; P2[4] = t.x; P2[5] = t.y; P2[6] = t.z; P2[7] = t.w;
+    t = rec[0 + h]; P0[4 * h] = t.x; P0[4 * h + 1] = t.y; P0[4 * h + 2] = t.z; P0[4 * h + 3] = t.w;
+    t = rec[2 + h]; P1[4 * h] = t.x; P1[4 * h + 1] = t.y; P1[4 * h + 2] = t.z; P1[4 * h + 3] = t.w;
+    t = rec[4 + h]; P2[4 * h] = t.x; P2[4 * h + 1] = t.y; P2[4 * h + 2] = t.z; P2[4 * h + 3] = t.w;
   }
   const float sx = reinterpret_cast<const float*>(smem + kOffScale)[cb >> 3];
   const int odd = lane & 1;  // 34*lane % 4 == 2*odd: odd lanes have aligned quants
   const uint32_t sel = odd ? 0x7654u : 0x5432u;
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    if (!((rowmask >> r) & 1)) continue;
-    const uint32_t* wp = reinterpret_cast<const uint32_t*>(stage + r * kQ8StageRow + ((34 * lane) & ~3));
-    uint32_t w[9];
-#pragma unroll
-    for (int u = 0; u < 9; ++u) w[u] = wp[u];
-    const float d = half_bits_to_float(odd ? (w[0] >> 16) : (w[0] & 0xFFFF));
-    int i0 = 0, i1 = 0, i2 = 0;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const uint32_t q = prmt(w[u], w[u + 1], sel);
-      i0 = dp4a_su(q, P0[u], i0);
-      i1 = dp4a_su(q, P1[u], i1);
-      i2 = dp4a_ss(q, P2[u], i2);
-    }
-    const float Jf = fmaf((float)i2, 65536.0f, fmaf((float)i1, 256.0f, (float)i0));
-    acc[r] = fmaf(d * sx, Jf, acc[r]);
+  for (int rp = 0; rp < 4; ++rp) {
+    if (2 * rp >= nslots) break;
+    acc[2 * rp] = q8_row(stage + (2 * rp) * kQ8StageRow, lane, P0, P1, P2, sx, sel, odd, acc[2 * rp]);
+    acc[2 * rp + 1] = q8_row(stage + (2 * rp + 1) * kQ8StageRow, lane, P0, P1, P2, sx, sel, odd, acc[2 * rp + 1]);
   }
 }
 
@@ -442,10 +465,12 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
   const unsigned G = gridDim.x;
 
   // the warp's stream of weight stages, one stage ahead of the compute
-  Cursor ic{0, -1, 0, 0};
+  Cursor ic;
+  ic.op = 0;
+  cursor_load(P, ic, cw);
   bool ic_ok = cursor_settle(P, ic, cw);
   if (ic_ok) {
-    issue_stage(P, ic, cw, lane, mybuf);
+    issue_stage(P, ic, lane, mybuf);
     cursor_advance(P, ic, cw);
     ic_ok = ic.op < P.n_ops;
   }
@@ -497,21 +522,19 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       prepare_x(op, smem, red, cw, lane, ctid);
       named_bar_sync(1, kConsumerThreads);
       const Geo g = geo_of(op);
-      const int64_t ngroups = (op.nrows + g.U - 1) / g.U;
-      int64_t g0, g1;
-      group_range(ngroups, g0, g1);
+      const Plan pl = plan_of(op, g, cw);
       float wbv = 0.0f;
       int wbi = -1;
-      for (int64_t wv = g0; wv + cw < g1; wv += kNumConsumerWarps) {
-        const int64_t r0 = (wv + cw) * g.U;
-        const int nr = (int)imin64(g.U, op.nrows - r0);
-        const uint32_t rowmask = g.pair ? (((1u << nr) - 1) * 0x11u) : ((1u << nr) - 1);
+      for (int grp = 0; grp < pl.ngroups; ++grp) {
+        const int64_t r0 = pl.r_lo + (int64_t)grp * g.U;
+        const int nr = (int)imin64(g.U, pl.r_hi - r0);
+        const int nslots = g.pair ? 8 : nr;
         float acc[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
         for (int s = 0; s < g.nslab; ++s) {
           if (ic_ok) {
-            issue_stage(P, ic, cw, lane, mybuf + ((j + 1) & 1) * kStageBytes);
+            issue_stage(P, ic, lane, mybuf + ((j + 1) & 1) * kStageBytes);
             cursor_advance(P, ic, cw);
             ic_ok = ic.op < P.n_ops;
             asm volatile("cp.async.wait_group 1;" ::: "memory");
@@ -522,9 +545,9 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           const uint8_t* stage = mybuf + (j & 1) * kStageBytes;
           const int nb = min(g.slab, g.bpr - s * g.slab);
           if (g.q8)
-            q8_slab(stage, smem, s * g.slab, nb, rowmask, lane, acc);
+            q8_slab(stage, smem, s * g.slab, nb, nslots, lane, acc);
           else
-            q4k_slab(stage, smem, s * g.slab, nb, rowmask, lane, acc);
+            q4k_slab(stage, smem, s * g.slab, nb, nslots, lane, acc);
           __syncwarp();
           ++j;
         }
@@ -586,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     if (ic_ok && P.sync) {
       Cursor pc = ic;
       for (int k = 0; k < kPrefetchStages && pc.op < P.n_ops; ++k) {
-        prefetch_stage_l2(P, pc, cw, lane);
+        prefetch_stage_l2(P, pc, lane);
         cursor_advance(P, pc, cw);
       }
     }
