@@ -43,13 +43,18 @@
 
 namespace {
 
-constexpr int kNumConsumerWarps = 8;
+#ifndef FAK_ENGINE_WARPS
+#define FAK_ENGINE_WARPS 16
+#endif
+constexpr int kNumConsumerWarps = FAK_ENGINE_WARPS;
+constexpr int kSlots = FAK_ENGINE_WARPS == 8 ? 8 : 4;  // weight row slots per stage
+constexpr int kLanesPerSlot = 32 / kSlots;
 constexpr int kThreads = 32 * kNumConsumerWarps;
 constexpr int kConsumerThreads = 32 * kNumConsumerWarps;
 constexpr int kStages = 2 * kNumConsumerWarps;   // two per warp
 constexpr int kPrefetchStages = 3;               // per warp, into L2, at a step boundary
-constexpr int kStageBytes = 9216;        // 8 rows x 8 Q4_K blocks x 144 B
-constexpr int kRowsPerGroup = 8;
+constexpr int kStageBytes = kSlots * 1152;       // row slots x 8 Q4_K blocks x 144 B
+constexpr int kRowsPerGroup = kSlots;
 constexpr int kQ4SlabBlocks = 8;         // Q4_K blocks per row per stage
 constexpr int kQ8SlabBlocks = 32;        // Q8_0 blocks per row per stage
 constexpr int kQ4StageRow = kQ4SlabBlocks * 144;  // 1152
@@ -115,7 +120,7 @@ __device__ __forceinline__ Geo geo_of(const EngOp& op) {
   Geo g;
   g.q8 = op.kind == OP_Q8;
   g.pair = op.kind == OP_Q4K_SWIGLU;
-  g.U = g.pair ? 4 : kRowsPerGroup;
+  g.U = g.pair ? kSlots / 2 : kRowsPerGroup;
   g.bpr = g.q8 ? op.K / 32 : op.K / 256;
   g.slab = g.q8 ? kQ8SlabBlocks : kQ4SlabBlocks;
   g.nslab = g.q8 ? (g.bpr + kQ8SlabBlocks - 1) / kQ8SlabBlocks : (g.bpr + kQ4SlabBlocks - 1) / kQ4SlabBlocks;
@@ -211,9 +216,9 @@ __device__ __forceinline__ const uint8_t* slot_src(const EngOp& op, const Geo& g
   const int64_t off = (int64_t)c.s * g.slab * g.blk;
   const int64_t row0 = c.r_lo + (int64_t)c.grp * g.U;
   if (g.pair) {
-    const int64_t row = row0 + (rl & 3);
+    const int64_t row = row0 + (rl % (kSlots / 2));
     if (row >= c.r_hi) return nullptr;
-    return op.w[rl >> 2] + row * row_bytes + off;
+    return op.w[rl / (kSlots / 2)] + row * row_bytes + off;
   }
   const int64_t row = row0 + rl;
   if (row >= c.r_hi) return nullptr;
@@ -221,24 +226,29 @@ __device__ __forceinline__ const uint8_t* slot_src(const EngOp& op, const Geo& g
 }
 
 // The whole warp copies one stage into `buf` and commits one cp.async group.
+// Lane l copies row slot l / kLanesPerSlot, 16-byte chunks t, t + kLanesPerSlot, ...
+// (t = l % kLanesPerSlot), so per-lane addresses advance by constants.
 __device__ void issue_stage(const EngParams& P, const Cursor& c, int lane, uint8_t* buf) {
   const EngOp& op = P.ops ? P.ops[c.op] : P.inl[c.op];
   const Geo g = geo_of(op);
   const int nb = min(g.slab, g.bpr - c.s * g.slab);
-  const int nch = nb * g.blk / 16;
-#pragma unroll 1
-  for (int rl = 0; rl < 8; ++rl) {
-    const uint8_t* src = slot_src(op, g, c, rl);
-    if (!src) continue;
-    uint8_t* dst = buf + rl * g.srow;
-    for (int ch = lane; ch < nch; ch += 32) cp_async16(dst + 16 * ch, src + 16 * ch);
+  const int nch = nb * g.blk / 16;  // <= 72
+  const int r = lane / kLanesPerSlot, t = lane % kLanesPerSlot;
+  const uint8_t* src = slot_src(op, g, c, r);
+  if (src) {
+    uint8_t* dst = buf + r * g.srow;
+#pragma unroll
+    for (int i = 0; i < (72 + kLanesPerSlot - 1) / kLanesPerSlot; ++i) {
+      const int ch = t + kLanesPerSlot * i;
+      if (ch < nch) cp_async16(dst + 16 * ch, src + 16 * ch);
+    }
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
 // Warm L2 with a stage's rows (one lane per row slot).
 __device__ void prefetch_stage_l2(const EngParams& P, const Cursor& c, int lane) {
-  if (lane >= 8) return;
+  if (lane >= kSlots) return;
   const EngOp& op = P.ops ? P.ops[c.op] : P.inl[c.op];
   const Geo g = geo_of(op);
   const uint8_t* src = slot_src(op, g, c, lane);
@@ -248,38 +258,43 @@ __device__ void prefetch_stage_l2(const EngParams& P, const Cursor& c, int lane)
 
 // ------------------------------------------------------------------ x preparation
 // Quantize x (optionally RMS-normalized) into the limb records in shared memory.
-__device__ void prepare_x(const EngOp& op, uint8_t* smem, float* red, int cw, int lane, int ctid) {
-  const int K = op.K;
+constexpr int kMaxSbPerWarp = (kMaxSuper + kNumConsumerWarps - 1) / kNumConsumerWarps;
+constexpr int kSbBatch = 2;  // super-blocks whose loads are in flight together
+
+// One pass over x: every load is issued first, then each super-block is
+// quantized and the warp's share of sum(x^2) is left in red[cw].  The
+// RMSNorm factor is a common scale of the whole vector, so it is applied to
+// the row results in the epilogue instead (the per-super-block power-of-two
+// scales keep the same relative precision either way).
+__device__ void prepare_x(const EngOp& op, uint8_t* smem, float* red, int cw, int lane) {
   const float* x = op.x;
-  float rn = 1.0f;
-  if (op.flags & F_NORM) {
-    float ss = 0.0f;
-    for (int i = ctid * 4; i < K; i += kConsumerThreads * 4) {
-      float4 v = ld_cg_f4(x + i);
-      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) red[cw] = ss;
-    named_bar_sync(1, kConsumerThreads);
-    float tot = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kNumConsumerWarps; ++w) tot += red[w];
-    rn = 1.0f / sqrtf(tot / (float)K + op.eps);
-  }
+  const int nsb = op.K / 256;
   uint8_t* xq = smem + kOffX;
   float* xS = reinterpret_cast<float*>(smem + kOffS);
   float* xsc = reinterpret_cast<float*>(smem + kOffScale);
-  const int nsb = K / 256;
-  for (int sb = cw; sb < nsb; sb += kNumConsumerWarps) {
-    const float* src = x + sb * 256 + lane * 8;
-    float4 a = ld_cg_f4(src), b = ld_cg_f4(src + 4);
-    float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float ss = 0.0f;
+#pragma unroll 1
+  for (int k0 = 0; k0 < kMaxSbPerWarp; k0 += kSbBatch) {
+  float4 va[kSbBatch], vb[kSbBatch];
+#pragma unroll
+  for (int k = 0; k < kSbBatch; ++k) {
+    const int sb = cw + (k0 + k) * kNumConsumerWarps;
+    if (sb < nsb) {
+      const float* src = x + sb * 256 + lane * 8;
+      va[k] = ld_cg_f4(src);
+      vb[k] = ld_cg_f4(src + 4);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kSbBatch; ++k) {
+    const int sb = cw + (k0 + k) * kNumConsumerWarps;
+    if (sb >= nsb) break;
+    const float v[8] = {va[k].x, va[k].y, va[k].z, va[k].w, vb[k].x, vb[k].y, vb[k].z, vb[k].w};
     float am = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      v[i] *= rn;
       am = fmaxf(am, fabsf(v[i]));
+      ss = fmaf(v[i], v[i], ss);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
@@ -317,6 +332,20 @@ __device__ void prepare_x(const EngOp& op, uint8_t* smem, float* red, int cw, in
     if ((lane & 3) == 0) xS[sb * 8 + (lane >> 2)] = sx * (float)xsum;
     if (lane == 0) xsc[sb] = sx;
   }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) red[cw] = ss;
+}
+
+// The RMSNorm factor from the warps' partial sums (same order in every thread
+// of every CTA, so every CTA gets the bitwise same factor).
+__device__ __forceinline__ float norm_factor(const EngOp& op, const float* red) {
+  if (!(op.flags & F_NORM)) return 1.0f;
+  float tot = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kNumConsumerWarps; ++w) tot += red[w];
+  return 1.0f / sqrtf(tot / (float)op.K + op.eps);
 }
 
 // ------------------------------------------------------------------ Q4_K slab
@@ -364,7 +393,7 @@ __device__ __forceinline__ float q4k_row(const uint8_t* base, const XRegs& x, in
 }
 
 __device__ __forceinline__ void q4k_slab(const uint8_t* stage, const uint8_t* smem, int jb0, int nb, int nslots,
-                                         int lane, float acc[8]) {
+                                         int lane, float acc[kSlots]) {
   const int b = lane >> 2, g = lane & 3;
   if (b >= nb) return;
   const int jb = jb0 + b;
@@ -389,7 +418,7 @@ __device__ __forceinline__ void q4k_slab(const uint8_t* stage, const uint8_t* sm
   const uint32_t sel = (uint32_t)(2 * g) | ((uint32_t)(2 * g + 1) << 4);
   const uint8_t* base = stage + b * 144;
 #pragma unroll
-  for (int rp = 0; rp < 4; ++rp) {
+  for (int rp = 0; rp < kSlots / 2; ++rp) {
     if (2 * rp >= nslots) break;
     acc[2 * rp] = q4k_row(base + (2 * rp) * kQ4StageRow, x, g, sel, acc[2 * rp]);
     acc[2 * rp + 1] = q4k_row(base + (2 * rp + 1) * kQ4StageRow, x, g, sel, acc[2 * rp + 1]);
@@ -419,7 +448,7 @@ __device__ __forceinline__ float q8_row(const uint8_t* rowbase, int lane, const 
 }
 
 __device__ __forceinline__ void q8_slab(const uint8_t* stage, const uint8_t* smem, int cb0, int nb, int nslots,
-                                        int lane, float acc[8]) {
+                                        int lane, float acc[kSlots]) {
   if (lane >= nb) return;
   const int cb = cb0 + lane;
   const uint4* rec = reinterpret_cast<const uint4*>(smem + kOffX + (cb >> 3) * kSuperBytes + (cb & 7) * kRecBytes);
@@ -435,7 +464,7 @@ __device__ __forceinline__ void q8_slab(const uint8_t* stage, const uint8_t* sme
   const int odd = lane & 1;  // 34*lane % 4 == 2*odd: odd lanes have aligned quants
   const uint32_t sel = odd ? 0x7654u : 0x5432u;
 #pragma unroll
-  for (int rp = 0; rp < 4; ++rp) {
+  for (int rp = 0; rp < kSlots / 2; ++rp) {
     if (2 * rp >= nslots) break;
     acc[2 * rp] = q8_row(stage + (2 * rp) * kQ8StageRow, lane, P0, P1, P2, sx, sel, odd, acc[2 * rp]);
     acc[2 * rp + 1] = q8_row(stage + (2 * rp + 1) * kQ8StageRow, lane, P0, P1, P2, sx, sel, odd, acc[2 * rp + 1]);
@@ -456,10 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const int ctid = threadIdx.x;
   const int cw = ctid >> 5, lane = ctid & 31;
-  float* red = reinterpret_cast<float*>(smem + kOffMisc);          // [8]
-  float* bestv = red + 8;                                           // [8]
-  int* besti = reinterpret_cast<int*>(red + 16);                    // [8]
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 96);
+  float* red = reinterpret_cast<float*>(smem + kOffMisc);          // [16]
+  float* bestv = red + 16;                                          // [16]
+  int* besti = reinterpret_cast<int*>(red + 32);                    // [16]
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 192);
   if (ctid == 0) *abort = 0;
   uint8_t* mybuf = smem + kOffRing + (2 * cw) * kStageBytes;
   const unsigned G = gridDim.x;
@@ -484,9 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       const unsigned target = (unsigned)i * G + (unsigned)op.wait_extra;
       if (ld_acquire_gpu(&P.sync[0]) < target) {
         const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_gpu(&P.sync[0]) < target) {
-          __nanosleep(32);
-          if (globaltimer_ns() - t0 > P.timeout_ns) {
+        for (uint32_t it = 1; ld_acquire_gpu(&P.sync[0]) < target; ++it) {
+          if ((it & 255) == 0 && globaltimer_ns() - t0 > P.timeout_ns) {
             set_error(P, FAK_ERR_TIMEOUT, abort);
             break;
           }
@@ -519,8 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         if (lane == 0 && P.tok_out) *P.tok_out = bi < 0 ? 0 : bi;
       }
     } else {
-      prepare_x(op, smem, red, cw, lane, ctid);
+      prepare_x(op, smem, red, cw, lane);
       named_bar_sync(1, kConsumerThreads);
+      const float rn = norm_factor(op, red);
       const Geo g = geo_of(op);
       const Plan pl = plan_of(op, g, cw);
       float wbv = 0.0f;
@@ -528,10 +557,10 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       for (int grp = 0; grp < pl.ngroups; ++grp) {
         const int64_t r0 = pl.r_lo + (int64_t)grp * g.U;
         const int nr = (int)imin64(g.U, pl.r_hi - r0);
-        const int nslots = g.pair ? 8 : nr;
-        float acc[8];
+        const int nslots = g.pair ? kSlots : nr;
+        float acc[kSlots];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
+        for (int r = 0; r < kSlots; ++r) acc[r] = 0.0f;
         for (int s = 0; s < g.nslab; ++s) {
           if (ic_ok) {
             issue_stage(P, ic, lane, mybuf + ((j + 1) & 1) * kStageBytes);
@@ -553,28 +582,28 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         }
         // fixed butterfly: every lane ends with the same-order-per-lane totals
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
+        for (int r = 0; r < kSlots; ++r) {
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
         }
         if (g.pair) {
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
+          for (int r = 0; r < kSlots / 2; ++r) {
             if (lane == r && r < nr) {
-              const float gt = acc[r], up = acc[4 + r];
+              const float gt = acc[r] * rn, up = acc[kSlots / 2 + r] * rn;
               op.y[0][r0 + r] = gt / (1.0f + expf(-gt)) * up;
             }
           }
         } else {
 #pragma unroll
-          for (int r = 0; r < 8; ++r) {
+          for (int r = 0; r < kSlots; ++r) {
             if (lane == r && r < nr) {
               const int64_t row = r0 + r;
               int seg = 0;
               int64_t seg_start = 0;
               while (seg < op.nseg - 1 && row >= op.seg_end[seg]) seg_start = op.seg_end[seg++];
               float* yp = op.y[seg] + (row - seg_start);
-              float v = acc[r];
+              float v = acc[r] * rn;
               if (op.flags & F_RESID) v += ld_cg_f(yp);
               if (op.flags & F_ARGMAX) {
                 if (P.logits) P.logits[row] = v;
@@ -585,8 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           }
           if (op.flags & F_ARGMAX) {
 #pragma unroll
-            for (int r = 0; r < 8; ++r)
-              if (r < nr) better(acc[r], (int)(r0 + r), wbv, wbi);
+            for (int r = 0; r < kSlots; ++r)
+              if (r < nr) better(acc[r] * rn, (int)(r0 + r), wbv, wbi);
           }
         }
       }
@@ -615,10 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     }
     // -- this CTA finished step i
     named_bar_sync(1, kConsumerThreads);
-    if (ctid == 0 && P.sync) {
-      __threadfence();
-      atomicAdd(&P.sync[0], 1u);
-    }
+    if (ctid == 0 && P.sync) red_release_gpu_add(&P.sync[0], 1u);
   }
   // nothing may still be landing in shared memory when the CTA exits
   asm volatile("cp.async.wait_all;" ::: "memory");

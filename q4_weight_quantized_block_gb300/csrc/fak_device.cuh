@@ -79,6 +79,12 @@ FAK_DEV uint32_t ld_acquire_gpu(const unsigned* p) {
   return v;
 }
 
+// Release-ordered add: this CTA's prior writes (made visible to thread 0 by
+// the barrier before it) happen-before any acquire that observes the sum.
+FAK_DEV void red_release_gpu_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 FAK_DEV float4 ld_cg_f4(const float* p) {
   float4 v;
   asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"
