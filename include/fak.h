@@ -93,6 +93,13 @@ const char* fak_version(void);
 int fak_q4k_pack(const float* w, int64_t N, int64_t K, void* out, size_t out_bytes);
 int fak_q8_0_pack(const float* w, int64_t N, int64_t K, void* out, size_t out_bytes);
 
+/* The same two quantizers on the GPU (one thread per block), for weights that
+ * are already in device memory: w and out are device pointers (w 4-byte
+ * aligned), asynchronous on `stream`.  The bytes equal the host packers' bit
+ * for bit.  Same shape rules and sizes as the host versions. */
+int fak_q4k_pack_device(const float* w, int64_t N, int64_t K, void* out, size_t out_bytes, fak_stream_t stream);
+int fak_q8_0_pack_device(const float* w, int64_t N, int64_t K, void* out, size_t out_bytes, fak_stream_t stream);
+
 /* ------------------------------------------------------------------ GEMV
  * y = W x for one activation vector ([diag] TL;DR: the Q4_K GEMV a decode
  * token runs per projection; section 4b: the single-GEMV benchmark).

@@ -46,6 +46,8 @@ _SIGS = {
     "fak_version": ([], ctypes.c_char_p),
     "fak_q4k_pack": ([P, I64, I64, P, SZ], I32),
     "fak_q8_0_pack": ([P, I64, I64, P, SZ], I32),
+    "fak_q4k_pack_device": ([P, I64, I64, P, SZ, P], I32),
+    "fak_q8_0_pack_device": ([P, I64, I64, P, SZ, P], I32),
     "fak_q4k_gemv": ([P, I64, I64, P, P, P], I32),
     "fak_q8_0_gemv": ([P, I64, I64, P, P, P], I32),
     "fak_q4k_gemv_batch": ([P, I64, I64, P, I32, P, P], I32),
@@ -118,6 +120,18 @@ def fak_q8_0_pack(w):
     out = np.empty((N, K // 32 * 34), dtype=np.uint8)
     _check(lib.fak_q8_0_pack(w.ctypes.data, N, K, out.ctypes.data, out.nbytes), "fak_q8_0_pack")
     return out
+
+
+def fak_q4k_pack_device(w, N, K, out, stream=None):
+    """Device f32 [N, K] (tensor or pointer) -> device Q4_K bytes `out` (N*(K/256)*144 bytes)."""
+    nbytes = N * (K // 256) * 144
+    _check(lib.fak_q4k_pack_device(_ptr(w), N, K, _ptr(out), nbytes, _stream(stream)), "fak_q4k_pack_device")
+
+
+def fak_q8_0_pack_device(w, N, K, out, stream=None):
+    """Device f32 [N, K] -> device Q8_0 bytes `out` (N*(K/32)*34 bytes)."""
+    nbytes = N * (K // 32) * 34
+    _check(lib.fak_q8_0_pack_device(_ptr(w), N, K, _ptr(out), nbytes, _stream(stream)), "fak_q8_0_pack_device")
 
 
 # ------------------------------------------------------------------ device calls

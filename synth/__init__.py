@@ -24,6 +24,8 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SO = os.path.join(_HERE, "_build", "libsynth.so")
 _lib = None
+_SO_CUDA = os.path.join(_HERE, "_build", "libsynth_cuda.so")
+_lib_cuda = None
 
 
 def build(force=False):
@@ -88,4 +90,35 @@ def to_bf16(a):
     a = np.ascontiguousarray(a, dtype=np.float32)
     out = np.empty(a.shape, dtype=np.uint16)
     _load().synth_f32_to_bf16(a.ctypes.data, out.ctypes.data, a.size)
+    return out
+
+
+def build_cuda(force=False):
+    """Compile synth_cuda.cu (the GPU twin of the generator) into _build/libsynth_cuda.so."""
+    src = os.path.join(_HERE, "synth_cuda.cu")
+    if force or not os.path.exists(_SO_CUDA) or os.path.getmtime(_SO_CUDA) < os.path.getmtime(src):
+        os.makedirs(os.path.dirname(_SO_CUDA), exist_ok=True)
+        tmp = _SO_CUDA + ".%d.tmp" % os.getpid()
+        nvcc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+        subprocess.check_call([nvcc if os.path.exists(nvcc) else "nvcc", "-gencode",
+                               "arch=compute_103a,code=sm_103a", "-O3", "-fmad=false", "-Xcompiler", "-fPIC",
+                               "-shared", src, "-o", tmp])
+        os.replace(tmp, _SO_CUDA)
+    return _SO_CUDA
+
+
+def normal_device(out, seed, tensor_id, sigma=1.0, start=0, stream=0):
+    """Fill a contiguous float32 CUDA tensor with elements start.. of tensor (seed, tensor_id),
+    generated on the GPU (same formula as the host; see synth_cuda.cu for the one caveat)."""
+    global _lib_cuda
+    if _lib_cuda is None:
+        lib = ctypes.CDLL(build_cuda())
+        lib.synth_normal_f32_device.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                                ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p]
+        lib.synth_normal_f32_device.restype = ctypes.c_int
+        _lib_cuda = lib
+    assert out.is_cuda and out.is_contiguous() and str(out.dtype) == "torch.float32"
+    rc = _lib_cuda.synth_normal_f32_device(seed, tensor_id, start, out.numel(), float(sigma), out.data_ptr(), stream)
+    if rc != 0:
+        raise RuntimeError("synth_normal_f32_device failed: CUDA error %d" % rc)
     return out
