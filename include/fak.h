@@ -143,6 +143,22 @@ int fak_mlp_decode(const void* Wgate, const void* Wup, const void* Wdown, int64_
                    const float* x, float eps, float* y, void* workspace, size_t workspace_bytes,
                    fak_stream_t stream);
 
+/* The same MLP for callers that cannot allocate device memory at call time
+ * (a host-side memory planner owns the device, or the call sits where an
+ * allocation's implicit synchronization is not allowed).  This entry point
+ * has no counterpart on the pages; it is a packaging of fak_mlp_decode.
+ * It allocates nothing: its scratch is a file-scope device array in the
+ * library, sized for d_ff <= FAK_MLP_NOALLOC_MAX_FF (about 74 KB), held on
+ * every GPU that loads the library until the process exits.  The first call
+ * on a device looks up that array's device address, so make that first call
+ * before any stream capture.  Larger d_ff returns FAK_ERR_SHAPE.  All calls
+ * share the one array: calls that overlap on the GPU (different streams, no
+ * ordering between them) race and give wrong results.  Other arguments,
+ * limits and results as fak_mlp_decode. */
+#define FAK_MLP_NOALLOC_MAX_FF 18432
+int fak_mlp_decode_noalloc(const void* Wgate, const void* Wup, const void* Wdown, int64_t d_model, int64_t d_ff,
+                           const float* x, float eps, float* y, fak_stream_t stream);
+
 /* ------------------------------------------------------------------ prefill GEMM
  * Y = X W^T for P tokens ([diag] section 2: mlp_gate_up_proj and mlp_down_proj
  * dominate prefill; section 4b: the q4k_gemm prefill kernel).

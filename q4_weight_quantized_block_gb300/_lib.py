@@ -16,6 +16,7 @@ lib = ctypes.CDLL(LIB_PATH)
 STATUS = {0: "FAK_OK", 1: "FAK_ERR_INVALID_ARG", 2: "FAK_ERR_SHAPE", 3: "FAK_ERR_ALIGN", 4: "FAK_ERR_CUDA",
           5: "FAK_ERR_TIMEOUT", 6: "FAK_ERR_NOMEM", 7: "FAK_ERR_DEVICE", 8: "FAK_ERR_UNSUPPORTED"}
 FAK_ENGINE_MAX_K = 18432
+FAK_MLP_NOALLOC_MAX_FF = 18432
 FAK_LAYER_GDN, FAK_LAYER_FA = 0, 1
 FAK_DECODE_ONE_LAUNCH, FAK_DECODE_PER_MATMUL = 0, 1
 
@@ -53,6 +54,7 @@ _SIGS = {
     "fak_q4k_gemv_batch": ([P, I64, I64, P, I32, P, P], I32),
     "fak_mlp_workspace_bytes": ([I64], SZ),
     "fak_mlp_decode": ([P, P, P, I64, I64, P, ctypes.c_float, P, P, SZ, P], I32),
+    "fak_mlp_decode_noalloc": ([P, P, P, I64, I64, P, ctypes.c_float, P, P], I32),
     "fak_q4k_gemm": ([P, I64, I64, P, I64, P, P], I32),
     "fak_swiglu_bf16": ([P, I64, I64, P, P], I32),
     "fak_decode_create": ([ctypes.POINTER(DecodeDesc), ctypes.POINTER(P)], I32),
@@ -156,6 +158,12 @@ def fak_mlp_decode(Wgate, Wup, Wdown, d_model, d_ff, x, eps, y, workspace, works
         workspace_bytes = workspace.numel() * workspace.element_size()
     _check(lib.fak_mlp_decode(_ptr(Wgate), _ptr(Wup), _ptr(Wdown), d_model, d_ff, _ptr(x), float(eps), _ptr(y),
                               _ptr(workspace), workspace_bytes, _stream(stream)), "fak_mlp_decode")
+
+
+def fak_mlp_decode_noalloc(Wgate, Wup, Wdown, d_model, d_ff, x, eps, y, stream=None):
+    """fak_mlp_decode with the library's own static scratch (no allocation; calls must not overlap)."""
+    _check(lib.fak_mlp_decode_noalloc(_ptr(Wgate), _ptr(Wup), _ptr(Wdown), d_model, d_ff, _ptr(x), float(eps),
+                                      _ptr(y), _stream(stream)), "fak_mlp_decode_noalloc")
 
 
 def fak_q4k_gemm(Wq, N, K, X, P_, Y, stream=None):

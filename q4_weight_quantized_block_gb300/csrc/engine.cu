@@ -824,6 +824,65 @@ extern "C" int fak_mlp_decode(const void* Wgate, const void* Wup, const void* Wd
   return launch_engine(P, sms, true, (cudaStream_t)stream);
 }
 
+// ------------------------------------------------------------------ MLP decode, no allocation
+// Some callers may not allocate device memory at call time: code running
+// under a memory planner that owns every byte of the device, code inside a
+// region where an allocation's implicit synchronization is not allowed, or a
+// host that simply has no allocator handle to pass in.  For them the batch-1
+// MLP has a variant whose scratch (two grid-sync counters and the SwiGLU
+// output) lives in this file-scope array, sized for d_ff up to
+// FAK_MLP_NOALLOC_MAX_FF.  Every GPU that loads the library holds it until the
+// process exits.  In host code the symbol is only a stand-in, so its device
+// address is looked up once per device (cudaGetSymbolAddress, with that device
+// current) and passed to the kernel.
+static __device__ __align__(256) uint8_t g_mlp_noalloc_scratch[256 + 4 * FAK_MLP_NOALLOC_MAX_FF];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+}  // namespace
+
+extern "C" int fak_mlp_decode_noalloc(const void* Wgate, const void* Wup, const void* Wdown, int64_t d_model,
+                                      int64_t d_ff, const float* x, float eps, float* y, fak_stream_t stream) {
+  if (!Wgate || !Wup || !Wdown || !x || !y) return FAK_ERR_INVALID_ARG;
+  if (d_model < 256 || d_model % 256 || d_model > FAK_ENGINE_MAX_K || d_ff < 256 || d_ff % 256 ||
+      d_ff > FAK_MLP_NOALLOC_MAX_FF)
+    return FAK_ERR_SHAPE;
+  if (!aligned16(Wgate) || !aligned16(Wup) || !aligned16(Wdown) || !aligned16(x)) return FAK_ERR_ALIGN;
+  int sms = 0;
+  int st = device_setup(&sms);
+  if (st != FAK_OK) return st;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fak_cuda_status(e);
+  if (dev < 0 || dev >= 64) return FAK_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      e = cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_mlp_noalloc_scratch);
+      if (e != cudaSuccess) {
+        g_noalloc_ptr[dev] = nullptr;
+        return fak_cuda_status(e);
+      }
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  unsigned* sync = static_cast<unsigned*>(scratch);
+  float* a = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + 256);
+  EngParams P = base_params();
+  P.inl[0] = make_matvec(OP_Q4K_SWIGLU, Wgate, d_ff, d_model, x, a, F_NORM);
+  P.inl[0].w[1] = static_cast<const uint8_t*>(Wup);
+  P.inl[0].eps = eps;
+  P.inl[1] = make_matvec(OP_Q4K, Wdown, d_model, d_ff, a, y, F_WAIT);
+  P.n_ops = 2;
+  P.sync = sync;
+  // the counters must start at zero; the SwiGLU output is fully overwritten
+  e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), (cudaStream_t)stream);
+  if (e != cudaSuccess) return fak_cuda_status(e);
+  return launch_engine(P, sms, true, (cudaStream_t)stream);
+}
+
 // ------------------------------------------------------------------ decode context
 struct fak_decode {
   fak_decode_desc desc;
