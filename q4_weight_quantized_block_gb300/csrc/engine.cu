@@ -43,11 +43,8 @@
 
 namespace {
 
-#ifndef FAK_ENGINE_WARPS
-#define FAK_ENGINE_WARPS 16
-#endif
-constexpr int kNumConsumerWarps = FAK_ENGINE_WARPS;
-constexpr int kSlots = FAK_ENGINE_WARPS == 8 ? 8 : 4;  // weight row slots per stage
+constexpr int kNumConsumerWarps = 12;
+constexpr int kSlots = 4;                         // weight row slots per stage
 constexpr int kLanesPerSlot = 32 / kSlots;
 constexpr int kThreads = 32 * kNumConsumerWarps;
 constexpr int kConsumerThreads = 32 * kNumConsumerWarps;
@@ -67,8 +64,9 @@ constexpr int kOffRing = 0;
 constexpr int kOffX = kOffRing + kStages * kStageBytes;           // 147456
 constexpr int kOffS = kOffX + kMaxSuper * kSuperBytes;            // +65664
 constexpr int kOffScale = kOffS + kMaxSuper * 8 * 4;
-constexpr int kOffBar = kOffScale + kMaxSuper * 4;
-constexpr int kOffMisc = kOffBar + 2 * kStages * 8;
+constexpr int kMaxUnits = 960;                    // (row group, slab) units per CTA in split mode
+constexpr int kOffPart = kOffScale + kMaxSuper * 4;
+constexpr int kOffMisc = kOffPart + kMaxUnits * kSlots * 4;
 constexpr int kSmemBytes = kOffMisc + 256;
 constexpr int kSmemAlloc = kSmemBytes + 128;
 
@@ -104,7 +102,6 @@ struct EngParams {
 
 __device__ int g_fak_status;  // status word of the stateless entry points
 
-__device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 
 struct Geo {
   int U;          // output rows per group
@@ -133,20 +130,46 @@ __device__ __forceinline__ bool has_weights(int kind) {
   return kind == OP_Q4K || kind == OP_Q4K_SWIGLU || kind == OP_Q8;
 }
 
-// Every warp of the grid owns a contiguous range of output rows of a step
-// (balanced to one row), processed as groups of U rows.
+// Work split of a step.  Each CTA owns a contiguous range of output rows,
+// cut into groups of U rows; a (group, slab) pair is a unit.  When the CTA has
+// at most kMaxUnits units ("split" mode) its warps take equal contiguous runs
+// of units, so a group's slabs may be shared by two or three warps; each warp
+// leaves one partial sum per segment (a maximal run of one group's slabs) in
+// shared memory and the groups are summed afterwards in slab order.  Larger
+// steps ("rows" mode) give every warp of the grid a contiguous range of rows,
+// balanced to one row, and its groups are finished by the warp itself.
 struct Plan {
-  int64_t r_lo, r_hi;
-  int ngroups;
+  int r_lo, r_hi;      // row window: the CTA's rows (split) or the warp's rows
+  int u0, u1;          // this warp's units; unit u is group u / nslab, slab u % nslab
+  int ngroups;         // groups in the window
+  int total;           // units of the CTA (split mode)
+  bool split;
 };
 
 __device__ __forceinline__ Plan plan_of(const EngOp& op, const Geo& g, int cw) {
-  const int64_t GW = (int64_t)gridDim.x * kNumConsumerWarps;
-  const int64_t gw = (int64_t)blockIdx.x * kNumConsumerWarps + cw;
   Plan p;
-  p.r_lo = op.nrows * gw / GW;
-  p.r_hi = op.nrows * (gw + 1) / GW;
-  p.ngroups = (int)((p.r_hi - p.r_lo + g.U - 1) / g.U);
+  const int64_t c = blockIdx.x, G = gridDim.x;
+  const int64_t R0 = op.nrows * c / G, R1 = op.nrows * (c + 1) / G;
+  const int64_t ng = (R1 - R0 + g.U - 1) / g.U;
+  const int64_t total = ng * g.nslab;
+  if (total <= kMaxUnits) {
+    p.split = true;
+    p.r_lo = (int)R0;
+    p.r_hi = (int)R1;
+    p.ngroups = (int)ng;
+    p.total = (int)total;
+    p.u0 = (int)(total * cw / kNumConsumerWarps);
+    p.u1 = (int)(total * (cw + 1) / kNumConsumerWarps);
+  } else {
+    const int64_t GW = G * kNumConsumerWarps, gw = c * kNumConsumerWarps + cw;
+    p.split = false;
+    p.r_lo = (int)(op.nrows * gw / GW);
+    p.r_hi = (int)(op.nrows * (gw + 1) / GW);
+    p.ngroups = (p.r_hi - p.r_lo + g.U - 1) / g.U;
+    p.total = 0;
+    p.u0 = 0;
+    p.u1 = p.ngroups * g.nslab;
+  }
   return p;
 }
 
@@ -161,99 +184,124 @@ __device__ __forceinline__ void set_error(const EngParams& P, int code, volatile
 // weights, for each of the warp's row groups, all slabs.
 struct Cursor {
   int op;          // step index, n_ops when exhausted
-  int grp;         // group within the warp's rows
-  int s;           // slab
-  int ngroups, nslab;
-  int64_t r_lo, r_hi;
+  int u, u1;       // current and end unit of the warp in this step
+  int grp, s;      // group and slab of unit u
+  int nslab;
+  int r_lo, r_hi;
+  // the step's descriptor fields the copies need, cached in registers when the
+  // cursor enters the step (reading the descriptor per stage is a slow chain)
+  const uint8_t* w0;
+  const uint8_t* w1;
+  const uint8_t* w2;
+  int se0, se1;     // segment row ends (rows >= se1 come from w2)
+  int row_bytes;    // bytes per weight row
+  int bpr;          // blocks per row
+  bool q8, pair;
+  // this lane's row slot in the current stage: source (NULL if the slot is empty)
+  // and 16-byte chunks to copy
+  const uint8_t* src;
+  int nch;
 };
 
-__device__ __forceinline__ void cursor_load(const EngParams& P, Cursor& c, int cw) {
-  c.grp = 0;
-  c.s = 0;
-  c.ngroups = 0;
+// Set src / nch of this lane's slot (row slot lane / kLanesPerSlot) for the cursor's unit.
+__device__ __forceinline__ void cursor_slot(Cursor& c, int lane) {
+  const int rl = lane / kLanesPerSlot;
+  const int slab = c.q8 ? kQ8SlabBlocks : kQ4SlabBlocks;
+  const int blk = c.q8 ? 34 : 144;
+  const int nb = min(slab, c.bpr - c.s * slab);
+  c.nch = nb * blk / 16;
+  const int64_t off = (int64_t)c.s * slab * blk;
+  const int row0 = c.r_lo + c.grp * (c.pair ? kSlots / 2 : kSlots);
+  c.src = nullptr;
+  if (c.pair) {
+    const int row = row0 + (rl % (kSlots / 2));
+    if (row < c.r_hi) c.src = (rl < kSlots / 2 ? c.w0 : c.w1) + (int64_t)row * c.row_bytes + off;
+    return;
+  }
+  const int row = row0 + rl;
+  if (row >= c.r_hi) return;
+  const uint8_t* w = row < c.se0 ? c.w0 : (row < c.se1 ? c.w1 : c.w2);
+  const int base = row < c.se0 ? 0 : (row < c.se1 ? c.se0 : c.se1);
+  c.src = w + (int64_t)(row - base) * c.row_bytes + off;
+}
+
+__device__ __forceinline__ void cursor_load(const EngParams& P, Cursor& c, int cw, int lane) {
+  c.u = c.u1 = 0;
   if (c.op >= P.n_ops) return;
   const EngOp& op = P.ops ? P.ops[c.op] : P.inl[c.op];
   if (!has_weights(op.kind)) return;
   const Geo g = geo_of(op);
   const Plan pl = plan_of(op, g, cw);
-  c.ngroups = pl.ngroups;
+  c.u = pl.u0;
+  c.u1 = pl.u1;
   c.nslab = g.nslab;
+  c.grp = pl.u0 / g.nslab;
+  c.s = pl.u0 - c.grp * g.nslab;
   c.r_lo = pl.r_lo;
   c.r_hi = pl.r_hi;
+  c.w0 = op.w[0];
+  c.w1 = op.w[1];
+  c.w2 = op.w[2];
+  c.se0 = op.nseg > 1 ? (int)op.seg_end[0] : 0x7fffffff;
+  c.se1 = op.nseg > 2 ? (int)op.seg_end[1] : 0x7fffffff;
+  c.row_bytes = g.bpr * g.blk;
+  c.bpr = g.bpr;
+  c.q8 = g.q8;
+  c.pair = g.pair;
+  if (c.u < c.u1) cursor_slot(c, lane);
 }
 
-__device__ __forceinline__ bool cursor_settle(const EngParams& P, Cursor& c, int cw) {
-  while (c.op < P.n_ops && c.grp >= c.ngroups) {
+__device__ __forceinline__ bool cursor_settle(const EngParams& P, Cursor& c, int cw, int lane) {
+  while (c.op < P.n_ops && c.u >= c.u1) {
     ++c.op;
-    cursor_load(P, c, cw);
+    cursor_load(P, c, cw, lane);
   }
   return c.op < P.n_ops;
 }
 
-__device__ __forceinline__ void cursor_advance(const EngParams& P, Cursor& c, int cw) {
-  if (++c.s >= c.nslab) {
+__device__ __forceinline__ void cursor_advance(const EngParams& P, Cursor& c, int cw, int lane) {
+  ++c.u;
+  if (c.u >= c.u1) {
+    cursor_settle(P, c, cw, lane);
+    return;
+  }
+  if (++c.s < c.nslab) {
+    // next slab of the same rows: only the offset and, for the last slab, the length change
+    const int slab = c.q8 ? kQ8SlabBlocks : kQ4SlabBlocks;
+    const int blk = c.q8 ? 34 : 144;
+    if (c.src) c.src += slab * blk;
+    c.nch = min(slab, c.bpr - c.s * slab) * blk / 16;
+  } else {
     c.s = 0;
     ++c.grp;
+    cursor_slot(c, lane);
   }
-  cursor_settle(P, c, cw);
-}
-
-// Source of output row `row` (segment lookup) at slab offset 0.
-__device__ __forceinline__ const uint8_t* row_src(const EngOp& op, int64_t row, int64_t row_bytes) {
-  int seg = 0;
-  int64_t seg_start = 0;
-  while (seg < op.nseg - 1 && row >= op.seg_end[seg]) seg_start = op.seg_end[seg++];
-  return op.w[seg] + (row - seg_start) * row_bytes;
 }
 
 FAK_DEV void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
-// Stage row slot rl: source (or NULL if empty) for the cursor's group and slab.
-__device__ __forceinline__ const uint8_t* slot_src(const EngOp& op, const Geo& g, const Cursor& c, int rl) {
-  const int64_t row_bytes = (int64_t)g.bpr * g.blk;
-  const int64_t off = (int64_t)c.s * g.slab * g.blk;
-  const int64_t row0 = c.r_lo + (int64_t)c.grp * g.U;
-  if (g.pair) {
-    const int64_t row = row0 + (rl % (kSlots / 2));
-    if (row >= c.r_hi) return nullptr;
-    return op.w[rl / (kSlots / 2)] + row * row_bytes + off;
-  }
-  const int64_t row = row0 + rl;
-  if (row >= c.r_hi) return nullptr;
-  return row_src(op, row, row_bytes) + off;
-}
-
 // The whole warp copies one stage into `buf` and commits one cp.async group.
 // Lane l copies row slot l / kLanesPerSlot, 16-byte chunks t, t + kLanesPerSlot, ...
 // (t = l % kLanesPerSlot), so per-lane addresses advance by constants.
-__device__ void issue_stage(const EngParams& P, const Cursor& c, int lane, uint8_t* buf) {
-  const EngOp& op = P.ops ? P.ops[c.op] : P.inl[c.op];
-  const Geo g = geo_of(op);
-  const int nb = min(g.slab, g.bpr - c.s * g.slab);
-  const int nch = nb * g.blk / 16;  // <= 72
+__device__ __forceinline__ void issue_stage(const Cursor& c, int lane, uint8_t* buf) {
   const int r = lane / kLanesPerSlot, t = lane % kLanesPerSlot;
-  const uint8_t* src = slot_src(op, g, c, r);
-  if (src) {
-    uint8_t* dst = buf + r * g.srow;
+  if (c.src) {
+    uint8_t* dst = buf + r * (c.q8 ? kQ8StageRow : kQ4StageRow);
 #pragma unroll
     for (int i = 0; i < (72 + kLanesPerSlot - 1) / kLanesPerSlot; ++i) {
       const int ch = t + kLanesPerSlot * i;
-      if (ch < nch) cp_async16(dst + 16 * ch, src + 16 * ch);
+      if (ch < c.nch) cp_async16(dst + 16 * ch, c.src + 16 * ch);
     }
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-// Warm L2 with a stage's rows (one lane per row slot).
-__device__ void prefetch_stage_l2(const EngParams& P, const Cursor& c, int lane) {
-  if (lane >= kSlots) return;
-  const EngOp& op = P.ops ? P.ops[c.op] : P.inl[c.op];
-  const Geo g = geo_of(op);
-  const uint8_t* src = slot_src(op, g, c, lane);
-  const int nb = min(g.slab, g.bpr - c.s * g.slab);
-  if (src) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"((uint32_t)(nb * g.blk)) : "memory");
+// Warm L2 with a stage's rows (the first lane of each row slot).
+__device__ __forceinline__ void prefetch_stage_l2(const Cursor& c, int lane) {
+  if (lane % kLanesPerSlot == 0 && c.src)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c.src), "r"((uint32_t)(c.nch * 16)) : "memory");
 }
 
 // ------------------------------------------------------------------ x preparation
@@ -358,40 +406,6 @@ struct XRegs {
   float SA, SB, sx16;
 };
 
-__device__ __forceinline__ float q4k_row(const uint8_t* base, const XRegs& x, int g, uint32_t sel, float acc) {
-  const uint4 h = *reinterpret_cast<const uint4*>(base);
-  const uint4 qa = *reinterpret_cast<const uint4*>(base + 16 + 32 * g);
-  const uint4 qb = *reinterpret_cast<const uint4*>(base + 32 + 32 * g);
-  const uint32_t sc_lo = h.y & 0x3F3F3F3Fu;
-  const uint32_t m_lo = h.z & 0x3F3F3F3Fu;
-  const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
-  const uint32_t m_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
-  const uint32_t scp = prmt(sc_lo, sc_hi, sel);
-  const uint32_t mp = prmt(m_lo, m_hi, sel);
-  const int scA16 = (int)(scp & 0xFF) << 4, scB = (int)((scp >> 8) & 0xFF);
-  const float mA = (float)(mp & 0xFF), mB = (float)((mp >> 8) & 0xFF);
-  const float d = half_bits_to_float(h.x & 0xFFFF), dmin = half_bits_to_float(h.x >> 16);
-  const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-  uint32_t a0 = 0, a1 = 0, b0 = 0, b1 = 0;
-  int a2 = 0, b2 = 0;
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const uint32_t lo = w[u] & 0x0F0F0F0Fu, hi = w[u] & 0xF0F0F0F0u;
-    a0 = dp4a_uu(lo, x.A0[u], a0);
-    a1 = dp4a_uu(lo, x.A1[u], a1);
-    a2 = dp4a_us(lo, x.A2[u], a2);
-    b0 = dp4a_uu(hi, x.B0[u], b0);
-    b1 = dp4a_uu(hi, x.B1[u], b1);
-    b2 = dp4a_us(hi, x.B2[u], b2);
-  }
-  const int J0 = (int)a0 * scA16 + (int)b0 * scB;
-  const int J1 = (int)a1 * scA16 + (int)b1 * scB;
-  const int J2 = a2 * scA16 + b2 * scB;
-  const float Jf = fmaf((float)J2, 65536.0f, fmaf((float)J1, 256.0f, (float)J0));
-  const float mterm = fmaf(mA, x.SA, mB * x.SB);
-  return fmaf(d * x.sx16, Jf, fmaf(-dmin, mterm, acc));
-}
-
 __device__ __forceinline__ void q4k_slab(const uint8_t* stage, const uint8_t* smem, int jb0, int nb, int nslots,
                                          int lane, float acc[kSlots]) {
   const int b = lane >> 2, g = lane & 3;
@@ -417,11 +431,51 @@ __device__ __forceinline__ void q4k_slab(const uint8_t* stage, const uint8_t* sm
   x.sx16 = reinterpret_cast<const float*>(smem + kOffScale)[jb] * 0.0625f;
   const uint32_t sel = (uint32_t)(2 * g) | ((uint32_t)(2 * g + 1) << 4);
   const uint8_t* base = stage + b * 144;
+  (void)nslots;
+  // all four row slots at once: 24 independent DP4A chains per quant word
+  uint4 h[4], qa[4], qb[4];
 #pragma unroll
-  for (int rp = 0; rp < kSlots / 2; ++rp) {
-    if (2 * rp >= nslots) break;
-    acc[2 * rp] = q4k_row(base + (2 * rp) * kQ4StageRow, x, g, sel, acc[2 * rp]);
-    acc[2 * rp + 1] = q4k_row(base + (2 * rp + 1) * kQ4StageRow, x, g, sel, acc[2 * rp + 1]);
+  for (int r = 0; r < 4; ++r) {
+    h[r] = *reinterpret_cast<const uint4*>(base + r * kQ4StageRow);
+    qa[r] = *reinterpret_cast<const uint4*>(base + r * kQ4StageRow + 16 + 32 * g);
+    qb[r] = *reinterpret_cast<const uint4*>(base + r * kQ4StageRow + 32 + 32 * g);
+  }
+  uint32_t a0[4], a1[4], b0[4], b1[4];
+  int a2[4], b2[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) a0[r] = a1[r] = b0[r] = b1[r] = 0, a2[r] = b2[r] = 0;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint32_t w = u < 4 ? (u == 0 ? qa[r].x : u == 1 ? qa[r].y : u == 2 ? qa[r].z : qa[r].w)
+                               : (u == 4 ? qb[r].x : u == 5 ? qb[r].y : u == 6 ? qb[r].z : qb[r].w);
+      const uint32_t lo = w & 0x0F0F0F0Fu, hi = w & 0xF0F0F0F0u;
+      a0[r] = dp4a_uu(lo, x.A0[u], a0[r]);
+      a1[r] = dp4a_uu(lo, x.A1[u], a1[r]);
+      a2[r] = dp4a_us(lo, x.A2[u], a2[r]);
+      b0[r] = dp4a_uu(hi, x.B0[u], b0[r]);
+      b1[r] = dp4a_uu(hi, x.B1[u], b1[r]);
+      b2[r] = dp4a_us(hi, x.B2[u], b2[r]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const uint32_t sc_lo = h[r].y & 0x3F3F3F3Fu;
+    const uint32_t m_lo = h[r].z & 0x3F3F3F3Fu;
+    const uint32_t sc_hi = (h[r].w & 0x0F0F0F0Fu) | ((h[r].y >> 2) & 0x30303030u);
+    const uint32_t m_hi = ((h[r].w >> 4) & 0x0F0F0F0Fu) | ((h[r].z >> 2) & 0x30303030u);
+    const uint32_t scp = prmt(sc_lo, sc_hi, sel);
+    const uint32_t mp = prmt(m_lo, m_hi, sel);
+    const int scA16 = (int)(scp & 0xFF) << 4, scB = (int)((scp >> 8) & 0xFF);
+    const float mA = (float)(mp & 0xFF), mB = (float)((mp >> 8) & 0xFF);
+    const float d = half_bits_to_float(h[r].x & 0xFFFF), dmin = half_bits_to_float(h[r].x >> 16);
+    const int J0 = (int)a0[r] * scA16 + (int)b0[r] * scB;
+    const int J1 = (int)a1[r] * scA16 + (int)b1[r] * scB;
+    const int J2 = a2[r] * scA16 + b2[r] * scB;
+    const float Jf = fmaf((float)J2, 65536.0f, fmaf((float)J1, 256.0f, (float)J0));
+    const float mterm = fmaf(mA, x.SA, mB * x.SB);
+    acc[r] = fmaf(d * x.sx16, Jf, fmaf(-dmin, mterm, acc[r]));
   }
 }
 
@@ -479,6 +533,68 @@ __device__ __forceinline__ void better(float v, int idx, float& bv, int& bi) {
   }
 }
 
+// The step's output fields, cached in registers once per step.
+struct EmitInfo {
+  float* y0;
+  float* y1;
+  float* y2;
+  int se0, se1;  // segment row ends
+  int flags;
+  float rn;      // RMSNorm factor (1 without F_NORM)
+  bool pair;
+};
+
+__device__ __forceinline__ EmitInfo emit_info(const EngOp& op, float rn) {
+  EmitInfo E;
+  E.y0 = op.y[0];
+  E.y1 = op.y[1];
+  E.y2 = op.y[2];
+  E.se0 = op.nseg > 1 ? (int)op.seg_end[0] : 0x7fffffff;
+  E.se1 = op.nseg > 2 ? (int)op.seg_end[1] : 0x7fffffff;
+  E.flags = op.flags;
+  E.rn = rn;
+  E.pair = op.kind == OP_Q4K_SWIGLU;
+  return E;
+}
+
+// Final value of output row `row`: RMSNorm factor, then the SwiGLU pair
+// (gate v, up v_up), or residual add + store, or logits + argmax candidate.
+__device__ __forceinline__ void emit(const EmitInfo& E, const EngParams& P, int row, float v, float v_up, float& wbv,
+                                     int& wbi) {
+  if (E.pair) {
+    const float gt = v * E.rn, up = v_up * E.rn;
+    E.y0[row] = gt / (1.0f + expf(-gt)) * up;
+    return;
+  }
+  float* yp = row < E.se0 ? E.y0 + row : (row < E.se1 ? E.y1 + (row - E.se0) : E.y2 + (row - E.se1));
+  float val = v * E.rn;
+  if (E.flags & F_RESID) val += ld_cg_f(yp);
+  if (E.flags & F_ARGMAX) {
+    if (P.logits) P.logits[row] = val;
+    better(val, row, wbv, wbi);
+  } else {
+    *yp = val;
+  }
+}
+
+// Sum the four row slots' partial sums over the warp with a fixed 6-shuffle
+// transpose: afterwards lanes 8r..8r+7 hold row r's total (lane 8r's value is
+// the one used, so results are bitwise reproducible).
+__device__ __forceinline__ float reduce4(const float (&acc)[kSlots], int lane) {
+  const bool h16 = lane & 16, h8 = lane & 8;
+  float k0 = h16 ? acc[2] : acc[0], k1 = h16 ? acc[3] : acc[1];
+  const float s0 = h16 ? acc[0] : acc[2], s1 = h16 ? acc[1] : acc[3];
+  k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+  k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+  float keep = h8 ? k1 : k0;
+  const float send = h8 ? k0 : k1;
+  keep += __shfl_xor_sync(0xffffffffu, send, 8);
+  keep += __shfl_xor_sync(0xffffffffu, keep, 4);
+  keep += __shfl_xor_sync(0xffffffffu, keep, 2);
+  keep += __shfl_xor_sync(0xffffffffu, keep, 1);
+  return keep;
+}
+
 // ------------------------------------------------------------------ the steps
 __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_constant__ EngParams P) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -496,11 +612,11 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
   // the warp's stream of weight stages, one stage ahead of the compute
   Cursor ic;
   ic.op = 0;
-  cursor_load(P, ic, cw);
-  bool ic_ok = cursor_settle(P, ic, cw);
+  cursor_load(P, ic, cw, lane);
+  bool ic_ok = cursor_settle(P, ic, cw, lane);
   if (ic_ok) {
-    issue_stage(P, ic, lane, mybuf);
-    cursor_advance(P, ic, cw);
+    issue_stage(ic, lane, mybuf);
+    cursor_advance(P, ic, cw, lane);
     ic_ok = ic.op < P.n_ops;
   }
   int j = 0;  // stages computed by this warp
@@ -552,74 +668,87 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       const float rn = norm_factor(op, red);
       const Geo g = geo_of(op);
       const Plan pl = plan_of(op, g, cw);
+      const EmitInfo E = emit_info(op, rn);
+      float* part = reinterpret_cast<float*>(smem + kOffPart);
+      const int nout = g.pair ? kSlots / 2 : kSlots;  // output rows per group slot set
       float wbv = 0.0f;
       int wbi = -1;
-      for (int grp = 0; grp < pl.ngroups; ++grp) {
-        const int64_t r0 = pl.r_lo + (int64_t)grp * g.U;
-        const int nr = (int)imin64(g.U, pl.r_hi - r0);
+      int grp = pl.u0 / g.nslab, s = pl.u0 - grp * g.nslab;
+      float acc[kSlots];
+#pragma unroll
+      for (int r = 0; r < kSlots; ++r) acc[r] = 0.0f;
+      for (int u = pl.u0; u < pl.u1; ++u) {
+        const int r0 = pl.r_lo + grp * g.U;
+        const int nr = min(g.U, pl.r_hi - r0);
         const int nslots = g.pair ? kSlots : nr;
-        float acc[kSlots];
-#pragma unroll
-        for (int r = 0; r < kSlots; ++r) acc[r] = 0.0f;
-        for (int s = 0; s < g.nslab; ++s) {
-          if (ic_ok) {
-            issue_stage(P, ic, lane, mybuf + ((j + 1) & 1) * kStageBytes);
-            cursor_advance(P, ic, cw);
-            ic_ok = ic.op < P.n_ops;
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-          } else {
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
-          }
-          __syncwarp();
-          const uint8_t* stage = mybuf + (j & 1) * kStageBytes;
-          const int nb = min(g.slab, g.bpr - s * g.slab);
-          if (g.q8)
-            q8_slab(stage, smem, s * g.slab, nb, nslots, lane, acc);
-          else
-            q4k_slab(stage, smem, s * g.slab, nb, nslots, lane, acc);
-          __syncwarp();
-          ++j;
-        }
-        // fixed butterfly: every lane ends with the same-order-per-lane totals
-#pragma unroll
-        for (int r = 0; r < kSlots; ++r) {
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
-        }
-        if (g.pair) {
-#pragma unroll
-          for (int r = 0; r < kSlots / 2; ++r) {
-            if (lane == r && r < nr) {
-              const float gt = acc[r] * rn, up = acc[kSlots / 2 + r] * rn;
-              op.y[0][r0 + r] = gt / (1.0f + expf(-gt)) * up;
-            }
-          }
+        if (ic_ok) {
+          issue_stage(ic, lane, mybuf + ((j + 1) & 1) * kStageBytes);
+          cursor_advance(P, ic, cw, lane);
+          ic_ok = ic.op < P.n_ops;
+          asm volatile("cp.async.wait_group 1;" ::: "memory");
         } else {
+          asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncwarp();
+        const uint8_t* stage = mybuf + (j & 1) * kStageBytes;
+        const int nb = min(g.slab, g.bpr - s * g.slab);
+        if (g.q8)
+          q8_slab(stage, smem, s * g.slab, nb, nslots, lane, acc);
+        else
+          q4k_slab(stage, smem, s * g.slab, nb, nslots, lane, acc);
+        __syncwarp();
+        ++j;
+        if (s == g.nslab - 1 || u == pl.u1 - 1) {
+          // end of a segment
+          const float v = reduce4(acc, lane);
+          const int rs = lane >> 3;  // the row slot this lane's value belongs to
+          if (pl.split) {
+            if ((lane & 7) == 0) part[u * kSlots + rs] = v;
+          } else {
+            const float up = __shfl_down_sync(0xffffffffu, v, 16);  // pair: up rows sit 16 lanes higher
+            if ((lane & 7) == 0 && rs < nout && rs < nr) emit(E, P, r0 + rs, v, up, wbv, wbi);
+          }
 #pragma unroll
-          for (int r = 0; r < kSlots; ++r) {
-            if (lane == r && r < nr) {
-              const int64_t row = r0 + r;
-              int seg = 0;
-              int64_t seg_start = 0;
-              while (seg < op.nseg - 1 && row >= op.seg_end[seg]) seg_start = op.seg_end[seg++];
-              float* yp = op.y[seg] + (row - seg_start);
-              float v = acc[r] * rn;
-              if (op.flags & F_RESID) v += ld_cg_f(yp);
-              if (op.flags & F_ARGMAX) {
-                if (P.logits) P.logits[row] = v;
-              } else {
-                *yp = v;
-              }
+          for (int r = 0; r < kSlots; ++r) acc[r] = 0.0f;
+        }
+        if (++s == g.nslab) {
+          s = 0;
+          ++grp;
+        }
+      }
+      if (pl.split) {
+        // sum each group's segments in slab order: the ends of warp runs inside the group, then the group end
+        named_bar_sync(1, kConsumerThreads);
+        for (int gi = ctid; gi < pl.ngroups; gi += kConsumerThreads) {
+          const int b0 = gi * g.nslab, e = b0 + g.nslab - 1;
+          float v[kSlots];
+#pragma unroll
+          for (int r = 0; r < kSlots; ++r) v[r] = 0.0f;
+          int last = -1;
+          for (int w = 0; w < kNumConsumerWarps - 1; ++w) {
+            const int bw = (int)((int64_t)pl.total * (w + 1) / kNumConsumerWarps) - 1;
+            if (bw >= b0 && bw < e && bw > last) {
+#pragma unroll
+              for (int r = 0; r < kSlots; ++r) v[r] += part[bw * kSlots + r];
+              last = bw;
             }
           }
-          if (op.flags & F_ARGMAX) {
 #pragma unroll
-            for (int r = 0; r < kSlots; ++r)
-              if (r < nr) better(acc[r] * rn, (int)(r0 + r), wbv, wbi);
-          }
+          for (int r = 0; r < kSlots; ++r) v[r] += part[e * kSlots + r];
+          const int r0 = pl.r_lo + gi * g.U;
+          const int nr = min(g.U, pl.r_hi - r0);
+#pragma unroll
+          for (int r = 0; r < kSlots; ++r)
+            if (r < nout && r < nr) emit(E, P, r0 + r, v[r], v[(r + kSlots / 2) % kSlots], wbv, wbi);
         }
       }
       if (op.flags & F_ARGMAX) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, wbv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, wbi, o);
+          better(ov, oi, wbv, wbi);
+        }
         if (lane == 0) {
           bestv[cw] = wbv;
           besti[cw] = wbi;
@@ -638,8 +767,8 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     if (ic_ok && P.sync) {
       Cursor pc = ic;
       for (int k = 0; k < kPrefetchStages && pc.op < P.n_ops; ++k) {
-        prefetch_stage_l2(P, pc, lane);
-        cursor_advance(P, pc, cw);
+        prefetch_stage_l2(pc, lane);
+        cursor_advance(P, pc, cw, lane);
       }
     }
     // -- this CTA finished step i
