@@ -48,7 +48,8 @@ constexpr int kSlots = 4;                         // weight row slots per stage
 constexpr int kLanesPerSlot = 32 / kSlots;
 constexpr int kThreads = 32 * kNumConsumerWarps;
 constexpr int kConsumerThreads = 32 * kNumConsumerWarps;
-constexpr int kStages = 2 * kNumConsumerWarps;   // two per warp
+constexpr int kBuffers = 3;                      // stage buffers per warp (two copies in flight)
+constexpr int kStages = kBuffers * kNumConsumerWarps;
 constexpr int kPrefetchStages = 3;               // per warp, into L2, at a step boundary
 constexpr int kStageBytes = kSlots * 1152;       // row slots x 8 Q4_K blocks x 144 B
 constexpr int kRowsPerGroup = kSlots;
@@ -57,18 +58,23 @@ constexpr int kQ8SlabBlocks = 32;        // Q8_0 blocks per row per stage
 constexpr int kQ4StageRow = kQ4SlabBlocks * 144;  // 1152
 constexpr int kQ8StageRow = kQ8SlabBlocks * 34;   // 1088
 constexpr int kMaxSuper = FAK_ENGINE_MAX_K / 256; // 72
-constexpr int kRecBytes = 112;           // one 32-element record: 3 x 32 limb bytes + 16 pad
-constexpr int kSuperBytes = 8 * kRecBytes + 16;   // 912: padding keeps lane accesses conflict-free
+// x limbs of one 256-element super-block: four 208-byte group records (group g
+// holds sub-blocks 2g and 2g+1: 3 x 32 limb bytes each, then 16 bytes of
+// padding); 832-byte super-blocks keep the Q4_K lanes' 16-byte reads free of
+// bank conflicts.
+constexpr int kGroupRec = 208;
+constexpr int kSuperBytes = 4 * kGroupRec;        // 832
 
 constexpr int kOffRing = 0;
-constexpr int kOffX = kOffRing + kStages * kStageBytes;           // 147456
-constexpr int kOffS = kOffX + kMaxSuper * kSuperBytes;            // +65664
+constexpr int kOffX = kOffRing + kStages * kStageBytes;
+constexpr int kOffS = kOffX + kMaxSuper * kSuperBytes;
 constexpr int kOffScale = kOffS + kMaxSuper * 8 * 4;
-constexpr int kMaxUnits = 960;                    // (row group, slab) units per CTA in split mode
+constexpr int kMaxUnits = 200;                    // (row group, slab) units per CTA in split mode
 constexpr int kOffPart = kOffScale + kMaxSuper * 4;
 constexpr int kOffMisc = kOffPart + kMaxUnits * kSlots * 4;
 constexpr int kSmemBytes = kOffMisc + 256;
 constexpr int kSmemAlloc = kSmemBytes + 128;
+static_assert(kSmemAlloc <= 232448, "engine shared memory exceeds the 227 KB per-block limit");
 
 enum OpKind { OP_Q4K = 0, OP_Q4K_SWIGLU = 1, OP_Q8 = 2, OP_EMBED = 3, OP_ARGMAX_REDUCE = 4 };
 enum OpFlag { F_NORM = 1, F_RESID = 2, F_WAIT = 4, F_ARGMAX = 8 };
@@ -371,7 +377,8 @@ __device__ void prepare_x(const EngOp& op, uint8_t* smem, float* red, int cw, in
         p2[h] |= (uint32_t)((xi >> 16) & 255) << (8 * i);
       }
     }
-    uint8_t* rec = xq + sb * kSuperBytes + (lane >> 2) * kRecBytes + (lane & 3) * 8;
+    const int j = lane >> 2;  // sub-block
+    uint8_t* rec = xq + sb * kSuperBytes + (j >> 1) * kGroupRec + (j & 1) * 96 + (lane & 3) * 8;
     *reinterpret_cast<uint2*>(rec) = make_uint2(p0[0], p0[1]);
     *reinterpret_cast<uint2*>(rec + 32) = make_uint2(p1[0], p1[1]);
     *reinterpret_cast<uint2*>(rec + 64) = make_uint2(p2[0], p2[1]);
@@ -411,9 +418,9 @@ __device__ __forceinline__ void q4k_slab(const uint8_t* stage, const uint8_t* sm
   const int b = lane >> 2, g = lane & 3;
   if (b >= nb) return;
   const int jb = jb0 + b;
-  const uint8_t* rec = smem + kOffX + jb * kSuperBytes + (2 * g) * kRecBytes;
+  const uint8_t* rec = smem + kOffX + jb * kSuperBytes + g * kGroupRec;
   const uint4* r0 = reinterpret_cast<const uint4*>(rec);
-  const uint4* r1 = reinterpret_cast<const uint4*>(rec + kRecBytes);
+  const uint4* r1 = reinterpret_cast<const uint4*>(rec + 96);
   XRegs x;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -505,7 +512,8 @@ __device__ __forceinline__ void q8_slab(const uint8_t* stage, const uint8_t* sme
                                         int lane, float acc[kSlots]) {
   if (lane >= nb) return;
   const int cb = cb0 + lane;
-  const uint4* rec = reinterpret_cast<const uint4*>(smem + kOffX + (cb >> 3) * kSuperBytes + (cb & 7) * kRecBytes);
+  const uint4* rec = reinterpret_cast<const uint4*>(smem + kOffX + (cb >> 3) * kSuperBytes +
+                                                    ((cb & 7) >> 1) * kGroupRec + (cb & 1) * 96);
   uint32_t P0[8], P1[8], P2[8];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -606,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
   int* besti = reinterpret_cast<int*>(red + 32);                    // [16]
   volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 192);
   if (ctid == 0) *abort = 0;
-  uint8_t* mybuf = smem + kOffRing + (2 * cw) * kStageBytes;
+  uint8_t* mybuf = smem + kOffRing + (kBuffers * cw) * kStageBytes;
   const unsigned G = gridDim.x;
 
   // the warp's stream of weight stages, one stage ahead of the compute
@@ -614,10 +622,17 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
   ic.op = 0;
   cursor_load(P, ic, cw, lane);
   bool ic_ok = cursor_settle(P, ic, cw, lane);
-  if (ic_ok) {
-    issue_stage(ic, lane, mybuf);
-    cursor_advance(P, ic, cw, lane);
-    ic_ok = ic.op < P.n_ops;
+  // two stages in flight before the first compute; every later iteration
+  // commits exactly one (possibly empty) group, so "wait_group 2" always
+  // means "this iteration's stage has landed"
+  for (int b = 0; b < kBuffers - 1; ++b) {
+    if (ic_ok) {
+      issue_stage(ic, lane, mybuf + b * kStageBytes);
+      cursor_advance(P, ic, cw, lane);
+      ic_ok = ic.op < P.n_ops;
+    } else {
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
   }
   int j = 0;  // stages computed by this warp
   __syncthreads();
@@ -682,15 +697,15 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         const int nr = min(g.U, pl.r_hi - r0);
         const int nslots = g.pair ? kSlots : nr;
         if (ic_ok) {
-          issue_stage(ic, lane, mybuf + ((j + 1) & 1) * kStageBytes);
+          issue_stage(ic, lane, mybuf + ((j + kBuffers - 1) % kBuffers) * kStageBytes);
           cursor_advance(P, ic, cw, lane);
           ic_ok = ic.op < P.n_ops;
-          asm volatile("cp.async.wait_group 1;" ::: "memory");
         } else {
-          asm volatile("cp.async.wait_group 0;" ::: "memory");
+          asm volatile("cp.async.commit_group;" ::: "memory");
         }
+        asm volatile("cp.async.wait_group 2;" ::: "memory");
         __syncwarp();
-        const uint8_t* stage = mybuf + (j & 1) * kStageBytes;
+        const uint8_t* stage = mybuf + (j % kBuffers) * kStageBytes;
         const int nb = min(g.slab, g.bpr - s * g.slab);
         if (g.q8)
           q8_slab(stage, smem, s * g.slab, nb, nslots, lane, acc);
