@@ -50,7 +50,6 @@ constexpr int kThreads = 32 * kNumConsumerWarps;
 constexpr int kConsumerThreads = 32 * kNumConsumerWarps;
 constexpr int kBuffers = 3;                      // stage buffers per warp (two copies in flight)
 constexpr int kStages = kBuffers * kNumConsumerWarps;
-constexpr int kPrefetchStages = 3;               // per warp, into L2, at a step boundary
 constexpr int kStageBytes = kSlots * 1152;       // row slots x 8 Q4_K blocks x 144 B
 constexpr int kRowsPerGroup = kSlots;
 constexpr int kQ4SlabBlocks = 8;         // Q4_K blocks per row per stage
@@ -567,16 +566,19 @@ __device__ __forceinline__ EmitInfo emit_info(const EngOp& op, float rn) {
 
 // Final value of output row `row`: RMSNorm factor, then the SwiGLU pair
 // (gate v, up v_up), or residual add + store, or logits + argmax candidate.
+__device__ __forceinline__ float* out_ptr(const EmitInfo& E, int row) {
+  return row < E.se0 ? E.y0 + row : (row < E.se1 ? E.y1 + (row - E.se0) : E.y2 + (row - E.se1));
+}
+
 __device__ __forceinline__ void emit(const EmitInfo& E, const EngParams& P, int row, float v, float v_up, float& wbv,
-                                     int& wbi) {
+                                     int& wbi, float res) {
   if (E.pair) {
     const float gt = v * E.rn, up = v_up * E.rn;
     E.y0[row] = gt / (1.0f + expf(-gt)) * up;
     return;
   }
-  float* yp = row < E.se0 ? E.y0 + row : (row < E.se1 ? E.y1 + (row - E.se0) : E.y2 + (row - E.se1));
-  float val = v * E.rn;
-  if (E.flags & F_RESID) val += ld_cg_f(yp);
+  float* yp = out_ptr(E, row);
+  const float val = v * E.rn + res;
   if (E.flags & F_ARGMAX) {
     if (P.logits) P.logits[row] = val;
     better(val, row, wbv, wbi);
@@ -639,6 +641,8 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
 
   for (int i = 0; i < P.n_ops; ++i) {
     const EngOp& op = P.ops ? P.ops[i] : P.inl[i];
+    if (P.ops && lane < 2 && i + 1 + lane < P.n_ops)  // the copy cursor reads them next
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(P.ops + i + 1 + lane));
     // -- wait for the previous step of this launch to finish on every CTA
     if (ctid == 0 && P.sync && (op.flags & F_WAIT) && (i > 0 || P.first_wait) && !*abort) {
       const unsigned target = (unsigned)i * G + (unsigned)op.wait_extra;
@@ -721,7 +725,8 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
             if ((lane & 7) == 0) part[u * kSlots + rs] = v;
           } else {
             const float up = __shfl_down_sync(0xffffffffu, v, 16);  // pair: up rows sit 16 lanes higher
-            if ((lane & 7) == 0 && rs < nout && rs < nr) emit(E, P, r0 + rs, v, up, wbv, wbi);
+            if ((lane & 7) == 0 && rs < nout && rs < nr)
+              emit(E, P, r0 + rs, v, up, wbv, wbi, (E.flags & F_RESID) ? ld_cg_f(out_ptr(E, r0 + rs)) : 0.0f);
           }
 #pragma unroll
           for (int r = 0; r < kSlots; ++r) acc[r] = 0.0f;
@@ -752,9 +757,13 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           for (int r = 0; r < kSlots; ++r) v[r] += part[e * kSlots + r];
           const int r0 = pl.r_lo + gi * g.U;
           const int nr = min(g.U, pl.r_hi - r0);
+          float res[kSlots];  // residuals loaded together: one L2 round trip, not four
 #pragma unroll
           for (int r = 0; r < kSlots; ++r)
-            if (r < nout && r < nr) emit(E, P, r0 + r, v[r], v[(r + kSlots / 2) % kSlots], wbv, wbi);
+            res[r] = ((E.flags & F_RESID) && r < nr) ? ld_cg_f(out_ptr(E, r0 + r)) : 0.0f;
+#pragma unroll
+          for (int r = 0; r < kSlots; ++r)
+            if (r < nout && r < nr) emit(E, P, r0 + r, v[r], v[(r + kSlots / 2) % kSlots], wbv, wbi, res[r]);
         }
       }
       if (op.flags & F_ARGMAX) {
@@ -776,14 +785,6 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           P.cand_val[blockIdx.x] = bv;
           P.cand_idx[blockIdx.x] = bi;
         }
-      }
-    }
-    // warm L2 with this warp's next stages while the grid waits at the step boundary
-    if (ic_ok && P.sync) {
-      Cursor pc = ic;
-      for (int k = 0; k < kPrefetchStages && pc.op < P.n_ops; ++k) {
-        prefetch_stage_l2(pc, lane);
-        cursor_advance(P, pc, cw, lane);
       }
     }
     // -- this CTA finished step i
