@@ -120,9 +120,18 @@ int fak_q8_0_gemv(const void* Wq, int64_t N, int64_t K, const float* x, float* y
 /* ------------------------------------------------------------------ batched GEMV
  * Y[m,:] = W X[m,:] for M activation rows against one resident weight
  * ([diag] section 4b: GEMVBatch, N GEMVs of one weight in one submission).
- *   X: device f32 [M, K] row-major, Y: device f32 [M, N]; 1 <= M <= 64.
- *   Other limits and the error bound as fak_q4k_gemv.  W is read from HBM
- *   once per call, not once per row.
+ *   X: device f32 [M, K] row-major, 16-byte aligned; Y: device f32 [M, N];
+ *   1 <= M <= 64; 1 <= N < 2^31; 256 <= K <= 2^24, K % 256 == 0.
+ *   W is read from HBM once per call, not once per row.  M == 1 is the
+ *   matrix-vector engine (fak_q4k_gemv, limits as there).  M >= 2 runs on
+ *   the tensor cores: x is split into two fp16 parts per 256-wide block with a
+ *   power-of-two scale, sc*q is exact in fp16, and the per-block scales d,
+ *   dmin are applied in f32, so the error bound is the f32 one of
+ *   fak_q4k_gemv for finite X.  Two launches (x split, then the GEMV); the
+ *   call takes a stream-ordered scratch of about 4*M'*K bytes (M' = M rounded
+ *   up to 8, 16, 32 or 64), plus 4*splits*M*N bytes when few row tiles force a
+ *   K split, from the device's default memory pool, and frees it on the same
+ *   stream.  Returns FAK_ERR_NOMEM if that allocation fails.
  */
 int fak_q4k_gemv_batch(const void* Wq, int64_t N, int64_t K, const float* X, int M, float* Y,
                        fak_stream_t stream);

@@ -913,17 +913,6 @@ extern "C" int fak_q8_0_gemv(const void* Wq, int64_t N, int64_t K, const float* 
   return single_matvec(OP_Q8, Wq, N, K, x, y, (cudaStream_t)stream);
 }
 
-extern "C" int fak_q4k_gemv_batch(const void* Wq, int64_t N, int64_t K, const float* X, int M, float* Y,
-                                  fak_stream_t stream) {
-  if (!X || !Y) return FAK_ERR_INVALID_ARG;
-  if (M < 1 || M > 64) return FAK_ERR_SHAPE;
-  for (int m = 0; m < M; ++m) {
-    int st = single_matvec(OP_Q4K, Wq, N, K, X + (int64_t)m * K, Y + (int64_t)m * N, (cudaStream_t)stream);
-    if (st != FAK_OK) return st;
-  }
-  return FAK_OK;
-}
-
 extern "C" int fak_device_status(fak_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return fak_cuda_status(e);
@@ -932,7 +921,8 @@ extern "C" int fak_device_status(fak_stream_t stream) {
   if (e != cudaSuccess) return fak_cuda_status(e);
   cudaMemcpyToSymbol(g_fak_status, &zero, sizeof(int));
   const int g = fak_gemm_take_status();
-  return v != 0 ? v : g;
+  const int b = fak_bgemv_take_status();
+  return v != 0 ? v : (g != 0 ? g : b);
 }
 
 // ------------------------------------------------------------------ MLP decode

@@ -150,3 +150,5 @@ static inline int fak_cuda_status(cudaError_t e) {
 
 // Reads and clears the prefill GEMM's device status word (host side, after a sync).
 int fak_gemm_take_status();
+// The same for the batched GEMV.
+int fak_bgemv_take_status();
