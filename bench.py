@@ -18,6 +18,10 @@ for the decode.  Multi-GPU runs (torchrun) are independent replicas: the
 decode step does not shard, each rank decodes its own stream.
 
   python bench.py [--steps K] [--warmup W] [--quick] [--impl reference]
+
+Profiling cases (not the headline): --layers L and --vocab V shrink the decode
+stack (the weights per token and the model shape change accordingly, and the
+line's config says so); --components picks the component sections to run.
 """
 import argparse
 import json
@@ -35,6 +39,7 @@ if ROOT not in sys.path:
 METRIC = "Q4_K GEMV GB/s (% HBM peak); 27B-shape decode-step tok/s; prefill TFLOPS"
 D, F, V, GI, QG, KV, NM, NL = 5120, 17408, 248320, 16480, 12288, 1024, 6144, 64
 SEED_DECODE = 3
+COMPONENTS = ("gemv", "mlp", "batch", "prefill")
 
 
 def parse_args():
@@ -45,7 +50,21 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline only, no component sections")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    return ap.parse_args()
+    ap.add_argument("--layers", type=int, default=NL, help="decode stack depth (profiling cases only)")
+    ap.add_argument("--vocab", type=int, default=V, help="lm_head rows (profiling cases only)")
+    ap.add_argument("--components", default="all",
+                    help="comma list of gemv,mlp,batch,prefill, or 'all' / 'none'")
+    a = ap.parse_args()
+    if a.quick:
+        a.components = "none"
+    a.components = set(COMPONENTS) if a.components == "all" else (
+        set() if a.components == "none" else set(a.components.split(",")))
+    bad = a.components - set(COMPONENTS)
+    if bad:
+        ap.error("unknown components: %s" % ",".join(sorted(bad)))
+    if a.vocab < 1 or a.layers < 1:
+        ap.error("--layers and --vocab must be positive")
+    return a
 
 
 def measured_peaks():
@@ -124,7 +143,7 @@ def q4k_device(fak, torch, seed, tid, n, k, scratch):
     return out
 
 
-def build_decode_model(fak, torch, n_layers=NL, seed=SEED_DECODE):
+def build_decode_model(fak, torch, n_layers=NL, vocab=V, seed=SEED_DECODE):
     """The 27B-shape stack: layer l % 4 == 3 is full-attention (q+gate, k, v, o), else GDN (in, out);
     every layer has gate/up/down; Q8_0 lm_head; f32 embedding.  Tensor ids 1000*l + slot."""
     import synth
@@ -141,14 +160,14 @@ def build_decode_model(fak, torch, n_layers=NL, seed=SEED_DECODE):
             L[key] = q4k_device(fak, torch, seed, 1000 * l + slot, n, k, scratch)
             q4_bytes += L[key].numel()
         layers.append(L)
-    lm = torch.empty(V * D // 32 * 34, dtype=torch.uint8, device="cuda")
+    lm = torch.empty(vocab * D // 32 * 34, dtype=torch.uint8, device="cuda")
     rows = F * D // D  # chunk of lm_head rows that fits the scratch buffer
-    for r0 in range(0, V, rows):
-        nr = min(rows, V - r0)
+    for r0 in range(0, vocab, rows):
+        nr = min(rows, vocab - r0)
         w = scratch[: nr * D]
         synth.normal_device(w, seed, 900000, 0.02, start=r0 * D)
         fak.fak_q8_0_pack_device(w, nr, D, lm[r0 * D // 32 * 34:(r0 + nr) * D // 32 * 34])
-    emb = torch.empty(V * D, dtype=torch.float32, device="cuda")
+    emb = torch.empty(vocab * D, dtype=torch.float32, device="cuda")
     synth.normal_device(emb, seed, 900001, 1.0)
     del scratch
     torch.cuda.synchronize()
@@ -169,8 +188,8 @@ def time_events(torch, fn, iters):
 
 # ------------------------------------------------------------------ headline: decode step
 def bench_decode(fak, torch, args, dist, rank, world):
-    layers, lm, emb, weight_bytes = build_decode_model(fak, torch)
-    ctx = fak.DecodeContext(D, F, V, GI, QG, KV, NM, layers, lm, emb, mode=fak.FAK_DECODE_ONE_LAUNCH)
+    layers, lm, emb, weight_bytes = build_decode_model(fak, torch, args.layers, args.vocab)
+    ctx = fak.DecodeContext(D, F, args.vocab, GI, QG, KV, NM, layers, lm, emb, mode=fak.FAK_DECODE_ONE_LAUNCH)
     tok = torch.zeros(1, dtype=torch.int32, device="cuda")
     for _ in range(args.warmup):
         ctx.step(tok, tok)
@@ -213,7 +232,7 @@ def bench_decode(fak, torch, args, dist, rank, world):
     e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
 
     # the same step launched once per matmul (the pages' per-command-buffer shape), for comparison
-    ctx_pm = fak.DecodeContext(D, F, V, GI, QG, KV, NM, layers, lm, emb, mode=fak.FAK_DECODE_PER_MATMUL)
+    ctx_pm = fak.DecodeContext(D, F, args.vocab, GI, QG, KV, NM, layers, lm, emb, mode=fak.FAK_DECODE_PER_MATMUL)
     for _ in range(2):
         ctx_pm.step(tok, tok)
     pm_ms = time_events(torch, lambda: ctx_pm.step(tok, tok), max(3, args.steps // 3))
@@ -280,110 +299,144 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------ components
-def bench_components(fak, torch, hbm, bf16):
+def graph_time(torch, fn, reps, iters=5):
+    """Device time per call of fn() (us) with host launch cost removed: `reps` calls captured in one CUDA
+    graph, replayed `iters` times, CUDA events on the replaying stream."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    del g
+    return e0.elapsed_time(e1) / (iters * reps) * 1e3
+
+
+def bench_components(fak, torch, hbm, bf16, which):
+    """Component sections.  GEMV-like calls are timed two ways: 'us' = device time per call back to back
+    (CUDA graph of many calls on rotating weight copies totalling > 4 x L2, so every call reads W from HBM),
+    'us_eager' = the same through the Python binding launch by launch (includes host launch cost)."""
     import synth
     out = {}
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")  # > L2 (129 MB)
 
-    def gemv_case(N, K, seed, wid, xid, copies):
-        scratch = torch.empty(N * K, dtype=torch.float32, device="cuda")
-        Ws = [q4k_device(fak, torch, seed, wid, N, K, scratch)]
+    def rotating(W, copies):
+        return [W] + [W.clone() for _ in range(copies - 1)]
+
+    if "gemv" in which:
+        def gemv_case(N, K, seed, wid, xid):
+            copies = max(1, min(60, int(600e6 // (N * K * 0.5625))))
+            scratch = torch.empty(N * K, dtype=torch.float32, device="cuda")
+            Ws = rotating(q4k_device(fak, torch, seed, wid, N, K, scratch), copies)
+            del scratch
+            x = torch.empty(K, device="cuda")
+            synth.normal_device(x, seed, xid, 1.0)
+            y = torch.empty(N, device="cuda")
+            it = [0]
+
+            def one():
+                fak.fak_q4k_gemv(Ws[it[0] % copies], N, K, x, y)
+                it[0] += 1
+            us = graph_time(torch, one, max(copies, 20) if copies > 1 else 5)
+            ue = time_events(torch, one, 50 if N * K < 100_000_000 else 10) * 1e3
+            byts = N * K // 256 * 144 + 4 * (N + K)
+            return {"N": N, "K": K, "us": us, "GBps": byts / us / 1e3, "frac": byts / us / 1e3 / hbm,
+                    "us_eager": ue, "rotating_copies": copies, "bytes": byts}
+
+        # single GEMV 5120 x 5120 (seed 0: W tensor 0, x tensor 1)
+        out["gemv_5120x5120"] = gemv_case(5120, 5120, 0, 0, 1)
+        # GEMV shape sweep (seed 4: W shape i -> tensor i, x -> 100 + i)
+        out["gemv_sweep"] = [gemv_case(N, K, 4, i, 100 + i) for i, (N, K) in
+                             enumerate([(1024, 5120), (5120, 5120), (17408, 5120), (5120, 17408), (248320, 5120)])]
+
+    if "mlp" in which or "batch" in which:
+        # batch-1 MLP weights (seed 1: x 0, gate 1, up 2, down 3), 4 rotating copies = 601 MB
+        scratch = torch.empty(F * D, dtype=torch.float32, device="cuda")
+        g = q4k_device(fak, torch, 1, 1, F, D, scratch)
+        u = q4k_device(fak, torch, 1, 2, F, D, scratch)
+        dn = q4k_device(fak, torch, 1, 3, D, F, scratch)
         del scratch
-        Ws += [Ws[0].clone() for _ in range(copies - 1)]
-        x = torch.empty(K, device="cuda")
-        synth.normal_device(x, seed, xid, 1.0)
-        y = torch.empty(N, device="cuda")
+        mlps = [(g, u, dn)] + [(g.clone(), u.clone(), dn.clone()) for _ in range(3)]
         it = [0]
+        if "mlp" in which:
+            x = torch.empty(D, device="cuda")
+            synth.normal_device(x, 1, 0, 1.0)
+            y = torch.empty(D, device="cuda")
+            ws = torch.empty(fak.fak_mlp_workspace_bytes(F), dtype=torch.uint8, device="cuda")
 
-        def one():
-            fak.fak_q4k_gemv(Ws[it[0] % copies], N, K, x, y)
-            it[0] += 1
-        for _ in range(5):
-            one()
-        ms = time_events(torch, one, 200 if N * K < 100_000_000 else 40)
-        singles = []
-        for _ in range(5):
-            flush.zero_()
-            singles.append(time_events(torch, one, 1))
-        byts = N * K // 256 * 144 + 4 * (N + K)
-        return {"N": N, "K": K, "us_back_to_back": ms * 1e3, "GBps": byts / ms / 1e6, "frac": byts / ms / 1e6 / hbm,
-                "us_single_cold": min(singles) * 1e3, "GBps_single": byts / min(singles) / 1e6,
-                "rotating_copies": copies, "bytes": byts}
+            def mlp():
+                a, b, c = mlps[it[0] % 4]
+                fak.fak_mlp_decode(a, b, c, D, F, x, 1e-6, y, ws)
+                it[0] += 1
+            us = graph_time(torch, mlp, 20)
+            ue = time_events(torch, mlp, 100) * 1e3
+            mb = 3 * F * D // 256 * 144 + 4 * (2 * D + F)
+            out["mlp_decode"] = {"us": us, "GBps": mb / us / 1e3, "frac": mb / us / 1e3 / hbm, "us_eager": ue,
+                                 "bytes": mb, "launches_per_call": 1}
+        if "batch" in which:
+            # batched GEMV sweep on the gate weight (seed 1, X tensor 4 rows 0..M-1)
+            Xall = torch.empty(64 * D, device="cuda")
+            synth.normal_device(Xall, 1, 4, 1.0)
+            bs = []
+            for M in (1, 2, 4, 8, 16, 32, 64):
+                Y = torch.empty(M * F, device="cuda")
 
-    # single GEMV 5120 x 5120 (seed 0: W tensor 0, x tensor 1); 40 rotating copies = 590 MB > 4 x L2
-    out["gemv_5120x5120"] = gemv_case(5120, 5120, 0, 0, 1, 40)
-    # GEMV shape sweep (seed 4: W shape i -> tensor i, x -> 100 + i)
-    sweep = []
-    for i, (N, K) in enumerate([(1024, 5120), (5120, 5120), (17408, 5120), (5120, 17408), (248320, 5120)]):
-        copies = max(1, int(600e6 // (N * K * 0.5625)))
-        sweep.append(gemv_case(N, K, 4, i, 100 + i, copies))
-    out["gemv_sweep"] = sweep
+                def bat():
+                    fak.fak_q4k_gemv_batch(mlps[it[0] % 4][0], F, D, Xall, M, Y)
+                    it[0] += 1
+                us = graph_time(torch, bat, 20)
+                ue = time_events(torch, bat, 20) * 1e3
+                byts = F * D // 256 * 144 + 4 * M * (D + F)
+                bs.append({"M": M, "us": us, "GBps": byts / us / 1e3, "frac": byts / us / 1e3 / hbm,
+                           "GFLOPs": 2.0 * M * F * D / us / 1e3, "us_per_row": us / M, "us_eager": ue})
+            out["gemv_batch_sweep"] = bs
+        del mlps, g, u, dn
 
-    # batch-1 MLP (seed 1: x 0, gate 1, up 2, down 3), 4 rotating copies = 601 MB
-    scratch = torch.empty(F * D, dtype=torch.float32, device="cuda")
-    g = q4k_device(fak, torch, 1, 1, F, D, scratch)
-    u = q4k_device(fak, torch, 1, 2, F, D, scratch)
-    dn = q4k_device(fak, torch, 1, 3, D, F, scratch)
-    del scratch
-    mlps = [(g, u, dn)] + [(g.clone(), u.clone(), dn.clone()) for _ in range(3)]
-    x = torch.empty(D, device="cuda")
-    synth.normal_device(x, 1, 0, 1.0)
-    y = torch.empty(D, device="cuda")
-    ws = torch.empty(fak.fak_mlp_workspace_bytes(F), dtype=torch.uint8, device="cuda")
-    it = [0]
-
-    def mlp():
-        a, b, c = mlps[it[0] % 4]
-        fak.fak_mlp_decode(a, b, c, D, F, x, 1e-6, y, ws)
-        it[0] += 1
-    for _ in range(3):
-        mlp()
-    ms = time_events(torch, mlp, 100)
-    mb = 3 * F * D // 256 * 144 + 4 * (2 * D + F)
-    out["mlp_decode"] = {"us": ms * 1e3, "GBps": mb / ms / 1e6, "frac": mb / ms / 1e6 / hbm, "bytes": mb,
-                         "launches_per_call": 1}
-    # batched GEMV sweep on the gate weight (seed 1, X tensor 4 rows 0..M-1)
-    Xall = torch.empty(64 * D, device="cuda")
-    synth.normal_device(Xall, 1, 4, 1.0)
-    bs = []
-    for M in (1, 2, 4, 8, 16, 32, 64):
-        Y = torch.empty(M * F, device="cuda")
-        ms = time_events(torch, lambda: fak.fak_q4k_gemv_batch(mlps[1][0], F, D, Xall, M, Y), 20)
-        byts = F * D // 256 * 144 + 4 * M * (D + F)
-        bs.append({"M": M, "us": ms * 1e3, "GBps": byts / ms / 1e6, "GFLOPs": 2.0 * M * F * D / ms / 1e6})
-    out["gemv_batch_sweep"] = bs
-    del mlps, g, u, dn
-
-    # prefill GEMMs (seed 2: W1 gate||up tensor 0, W2 down tensor 1, X tensor 2)
-    scratch = torch.empty(2 * F * D, dtype=torch.float32, device="cuda")
-    W1 = q4k_device(fak, torch, 2, 0, 2 * F, D, scratch)
-    W2 = q4k_device(fak, torch, 2, 1, D, F, scratch)
-    Xf = scratch[: 1024 * D]
-    synth.normal_device(Xf, 2, 2, 1.0)
-    X = Xf.view(1024, D).to(torch.bfloat16)
-    del scratch, Xf
-    pre = []
-    for P in (256, 512, 1024):
-        Y1 = torch.empty(P * 2 * F, device="cuda")
-        X2 = torch.empty(P * F, dtype=torch.bfloat16, device="cuda")
-        Y2 = torch.empty(P * D, device="cuda")
-        m1 = time_events(torch, lambda: fak.fak_q4k_gemm(W1, 2 * F, D, X, P, Y1), 10)
-        ms_sw = time_events(torch, lambda: fak.fak_swiglu_bf16(Y1, P, F, X2), 10)
-        m2 = time_events(torch, lambda: fak.fak_q4k_gemm(W2, D, F, X2, P, Y2), 10)
-        f1, f2 = 2.0 * P * 2 * F * D, 2.0 * P * D * F
-        pre.append({"P": P, "gate_up_ms": m1, "gate_up_TFLOPs": f1 / m1 / 1e9, "gate_up_frac": f1 / m1 / 1e9 / bf16,
-                    "swiglu_ms": ms_sw, "down_ms": m2, "down_TFLOPs": f2 / m2 / 1e9, "down_frac": f2 / m2 / 1e9 / bf16,
-                    "total_TFLOPs": (f1 + f2) / (m1 + ms_sw + m2) / 1e9})
-    out["prefill_gemm"] = pre
+    if "prefill" in which:
+        # prefill GEMMs (seed 2: W1 gate||up tensor 0, W2 down tensor 1, X tensor 2)
+        scratch = torch.empty(2 * F * D, dtype=torch.float32, device="cuda")
+        W1 = q4k_device(fak, torch, 2, 0, 2 * F, D, scratch)
+        W2 = q4k_device(fak, torch, 2, 1, D, F, scratch)
+        Xf = scratch[: 1024 * D]
+        synth.normal_device(Xf, 2, 2, 1.0)
+        X = Xf.view(1024, D).to(torch.bfloat16)
+        del scratch, Xf
+        pre = []
+        for P in (256, 512, 1024):
+            Y1 = torch.empty(P * 2 * F, device="cuda")
+            X2 = torch.empty(P * F, dtype=torch.bfloat16, device="cuda")
+            Y2 = torch.empty(P * D, device="cuda")
+            m1 = time_events(torch, lambda: fak.fak_q4k_gemm(W1, 2 * F, D, X, P, Y1), 10)
+            ms_sw = time_events(torch, lambda: fak.fak_swiglu_bf16(Y1, P, F, X2), 10)
+            m2 = time_events(torch, lambda: fak.fak_q4k_gemm(W2, D, F, X2, P, Y2), 10)
+            f1, f2 = 2.0 * P * 2 * F * D, 2.0 * P * D * F
+            pre.append({"P": P, "gate_up_ms": m1, "gate_up_TFLOPs": f1 / m1 / 1e9,
+                        "gate_up_frac": f1 / m1 / 1e9 / bf16, "swiglu_ms": ms_sw, "down_ms": m2,
+                        "down_TFLOPs": f2 / m2 / 1e9, "down_frac": f2 / m2 / 1e9 / bf16,
+                        "total_TFLOPs": (f1 + f2) / (m1 + ms_sw + m2) / 1e9})
+        out["prefill_gemm"] = pre
     st = fak.fak_device_status()
     if st != 0:
         raise RuntimeError("component status %d" % st)
     return out
 
 
-# the dram bytes of one decode launch from the ncu capture summarised under profiles/
-# (engine kernel, 4-layer stack scaled by weight bytes); None until measured for this kernel version
-DECODE_TRAFFIC_BYTES = None
+# dram bytes (read + write) of one full decode launch: the ncu capture of the same engine kernel on the
+# 4-layer stack (profiles/engine_kernel_decode_27b_step.md: 950.73 MB for 945.22 MB of weights), scaled by
+# weight bytes to the 15.048 GB step.  Set to None whenever the engine kernel changes until re-captured.
+DECODE_TRAFFIC_BYTES = int(950.728448e6 / 945.22368e6 * (15_048_048_640 + 5120 * 4))
 
 
 def main():
@@ -406,8 +459,8 @@ def main():
     hbm, bf16, bf16_sus, peak_src = measured_peaks()
     dec = bench_decode(fak, torch, args, dist, rank, world)
     comps = None
-    if rank == 0 and not args.quick:
-        comps = bench_components(fak, torch, hbm, bf16)
+    if rank == 0 and args.components:
+        comps = bench_components(fak, torch, hbm, bf16, args.components)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         bps, dt, threads, desc = cpu_oracle_sample()
@@ -418,19 +471,23 @@ def main():
     if rank != 0:
         return
     achieved = dec["algo_bytes"] / (dec["ms"] * 1e-3) / 1e9
+    full = args.layers == NL and args.vocab == V
+    workload = ("27B-shape hybrid decode step, batch 1: 64 layers (48 GDN: in 5120->16480, out 6144->5120; 16 FA: "
+                "q+gate 5120->12288, k/v 5120->1024, o 6144->5120; MLP 5120->2x17408->5120), RMSNorm, SwiGLU, "
+                "Q8_0 lm_head 5120->248320 + argmax") if full else (
+        "REDUCED profiling case of the 27B-shape decode step: %d layers, Q8_0 lm_head 5120->%d (not the headline)"
+        % (args.layers, args.vocab))
     line = {
         "metric": METRIC, "value": dec["tok_s"], "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dec["ms"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32",
         "data": "synthetic: seeded N(0,0.02^2) weights quantized to Q4_K / Q8_0 on the GPU, N(0,1) embedding",
-        "config": {"workload": "27B-shape hybrid decode step, batch 1: 64 layers (48 GDN: in 5120->16480, out "
-                               "6144->5120; 16 FA: q+gate 5120->12288, k/v 5120->1024, o 6144->5120; MLP "
-                               "5120->2x17408->5120), RMSNorm, SwiGLU, Q8_0 lm_head 5120->248320 + argmax",
+        "config": {"workload": workload,
                    "weights_bytes_per_token": dec["algo_bytes"], "launch": "one kernel per token",
-                   "l2": "weights per token 15.05 GB >> L2 129 MB: no flush needed",
+                   "l2": "weights per token %.2f GB >> L2 129 MB: no flush needed" % (dec["algo_bytes"] / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": DECODE_TRAFFIC_BYTES, "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": DECODE_TRAFFIC_BYTES if full else None, "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)",
                      "kernel": "engine_kernel (one-launch decode step)"},
         "cpu_baseline": cpu,
         "e2e": {"value": dec["e2e_tok_s"], "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
