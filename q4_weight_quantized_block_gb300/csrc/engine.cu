@@ -637,6 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     }
   }
   int j = 0;  // stages computed by this warp
+  // set when the warp issued its next stage early, at the end of its previous step
+  // (three copies in flight through the grid-wide wait); the next unit then skips
+  // its own issue, so "wait_group 2" still means "this unit's stage has landed"
+  bool ahead = false;
   __syncthreads();
 
   for (int i = 0; i < P.n_ops; ++i) {
@@ -700,7 +704,9 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         const int r0 = pl.r_lo + grp * g.U;
         const int nr = min(g.U, pl.r_hi - r0);
         const int nslots = g.pair ? kSlots : nr;
-        if (ic_ok) {
+        if (ahead) {
+          ahead = false;
+        } else if (ic_ok) {
           issue_stage(ic, lane, mybuf + ((j + kBuffers - 1) % kBuffers) * kStageBytes);
           cursor_advance(P, ic, cw, lane);
           ic_ok = ic.op < P.n_ops;
@@ -735,6 +741,14 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           s = 0;
           ++grp;
         }
+      }
+      // the warp is done with this step's stages: the buffer of its last one is free,
+      // so the next step's third stage starts loading now, before the grid-wide wait
+      if (!ahead && ic_ok && pl.u1 > pl.u0) {
+        issue_stage(ic, lane, mybuf + ((j + kBuffers - 1) % kBuffers) * kStageBytes);
+        cursor_advance(P, ic, cw, lane);
+        ic_ok = ic.op < P.n_ops;
+        ahead = true;
       }
       if (pl.split) {
         // sum each group's segments in slab order: the ends of warp runs inside the group, then the group end
