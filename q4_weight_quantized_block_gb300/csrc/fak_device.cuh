@@ -42,17 +42,29 @@ FAK_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about `hint_ns` pass, instead of spinning and taking issue
+// slots from the warps that share its scheduler.
+FAK_DEV bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait on an mbarrier phase.  Gives up when `abort` becomes non-zero
-// or after `timeout_ns`; returns false then.
+// or after `timeout_ns`; returns false then.  Between checks the thread is
+// suspended (at most ~20 us per check).
 FAK_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort, uint64_t timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63) == 63) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > timeout_ns) return false;
-    }
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
   }
 }
 

@@ -10,8 +10,11 @@
 //   warp 0      TMA producer: X tile [256 tokens x 64] bf16, 128-byte swizzle
 //   warp 1      TMEM owner + MMA issuer: 4 x tcgen05.mma (M128 N256 K16) per stage
 //   warps 2-5   dequant producers: 128 W rows x 64 weights -> bf16, written in the
-//               same 128-byte-swizzled K-major layout (one thread per row)
+//               same 128-byte-swizzled K-major layout (one thread per row, reading
+//               its row's Q4_K block from the W ring in shared memory)
 //   warps 6-9   epilogue: tcgen05.ld of the f32 accumulator -> Y (coalesced)
+//   warp 10     TMA producer (W): the 128-row x 144-byte Q4_K tile of each
+//               super-block into a two-slot ring, two super-blocks ahead
 // Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile overlap
 // the MMAs of the next.  Every wait is bounded; on a timeout the kernel records
 // FAK_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
@@ -32,13 +35,16 @@ namespace {
 constexpr int BM = 128;  // weight rows per tile (MMA M)
 constexpr int BN = 256;  // tokens per tile (MMA N)
 constexpr int BK = 64;   // K per stage (one 128-byte swizzle atom of bf16)
-constexpr int kStagesG = 4;
-constexpr int kThreadsG = 320;
+constexpr int kStagesG = 3;
+constexpr int kThreadsG = 352;
+constexpr int kWSlots = 2;                // W super-block tiles in flight
+constexpr int kWTile = 128 * 144;       // 128 rows x 144 bytes
 constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kBBytes = BN * BK * 2;  // 32 KB
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kStagesG * kABytes;
-constexpr int kOffBarG = kOffB + kStagesG * kBBytes;
+constexpr int kOffW = kOffB + kStagesG * kBBytes;
+constexpr int kOffBarG = kOffW + kWSlots * kWTile;
 constexpr int kSmemG = kOffBarG + 256;
 constexpr int kSmemAllocG = kSmemG + 1024;
 constexpr uint32_t kTmemCols = 512;
@@ -83,6 +89,14 @@ FAK_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint
       : "memory");
 }
 
+FAK_DEV void tma_load_2d_hint(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
 FAK_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%"
@@ -106,9 +120,8 @@ struct GemmParams {
 // Dequantize the 64 weights of one row for K step g (0..3 within a super-block):
 // low nibbles of qs[32g..32g+31] are k 0..31 (sub-block 2g), high nibbles k 32..63
 // (sub-block 2g+1).  w = d*sc*q - dmin*m, rounded once to bf16.
-// `blk` holds the row's 144-byte block as 9 uint4.
-FAK_DEV void dequant_row_step(const uint4 (&blk)[9], int g, uint8_t* row_smem, int r8) {
-  const uint4 h = blk[0];
+// `h` is the row's 16-byte block header, q0 / q1 the 32 quant bytes of step g.
+FAK_DEV void dequant_row_step(const uint4 h, const uint4 q0, const uint4 q1, int g, uint8_t* row_smem, int r8) {
   const uint32_t sc_lo = h.y & 0x3F3F3F3Fu, m_lo = h.z & 0x3F3F3F3Fu;
   const uint32_t sc_hi = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
   const uint32_t m_hi = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
@@ -124,7 +137,6 @@ FAK_DEV void dequant_row_step(const uint4 (&blk)[9], int g, uint8_t* row_smem, i
     mul[hsel] = 32.0f * a;
     add[hsel] = -(16.0f * a + b);
   }
-  const uint4 q0 = blk[1 + 2 * g], q1 = blk[2 + 2 * g];
   const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
   for (int hsel = 0; hsel < 2; ++hsel) {
@@ -153,7 +165,8 @@ FAK_DEV void dequant_row_step(const uint4 (&blk)[9], int g, uint8_t* row_smem, i
 }
 
 __global__ void __launch_bounds__(kThreadsG, 1)
-    q4k_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ GemmParams p) {
+    q4k_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+                    const __grid_constant__ GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_x = reinterpret_cast<uint64_t*>(smem + kOffBarG);
@@ -162,7 +175,9 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   uint64_t* tfull = empty + kStagesG;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* wfull = drain + 1;
+  uint64_t* wempty = wfull + kWSlots;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty + kWSlots);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -177,6 +192,10 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       mbar_init(&tempty[a], 4);
     }
     mbar_init(drain, 1);
+    for (int w = 0; w < kWSlots; ++w) {
+      mbar_init(&wfull[w], 1);
+      mbar_init(&wempty[w], 4);
+    }
     *abort = 0;
     fence_mbar_init();
   }
@@ -265,25 +284,28 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     // ---------------- dequant producers: thread t owns row t of each W tile
     const int t = threadIdx.x - 64;
     const int r8 = t & 7;
-    const int64_t row_bytes = p.K / 256 * 144;
-    int it = 0;
-    for (int tile = blockIdx.x; tile < total_tiles && !*abort; tile += gridDim.x) {
-      const int64_t n = (int64_t)(tile / p.n_tiles_p) * BM + t;
-      const uint4* src = reinterpret_cast<const uint4*>(p.W + n * row_bytes);
-      uint4 blk[9], nxt[9];
-#pragma unroll
-      for (int i = 0; i < 9; ++i) nxt[i] = __ldg(src + i);
-      bool ok = true;
+    int it = 0, wq = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total_tiles && ok && !*abort; tile += gridDim.x) {
+      uint4 hdr = make_uint4(0, 0, 0, 0);
+      const uint8_t* rowp = nullptr;
       for (int kt = 0; kt < ktiles && ok; ++kt, ++it) {
         const int g = kt & 3;
         if (g == 0) {
-#pragma unroll
-          for (int i = 0; i < 9; ++i) blk[i] = nxt[i];
-          if (kt + 4 < ktiles) {
-            const uint4* s2 = src + (kt / 4 + 1) * 9;
-#pragma unroll
-            for (int i = 0; i < 9; ++i) nxt[i] = __ldg(s2 + i);
+          if (!mbar_wait_bounded(&wfull[wq % kWSlots], (wq / kWSlots) & 1, abort, tmo)) {
+            if (!*abort) fail();
+            ok = false;
+            break;
           }
+          rowp = smem + kOffW + (wq % kWSlots) * kWTile + t * 144;
+          hdr = *reinterpret_cast<const uint4*>(rowp);
+        }
+        const uint4 q0 = *reinterpret_cast<const uint4*>(rowp + 16 + 32 * g);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(rowp + 32 + 32 * g);
+        if (g == 3) {  // this super-block's W tile is fully read
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&wempty[wq % kWSlots]);
+          ++wq;
         }
         const int s = it % kStagesG;
         if (it >= kStagesG && !mbar_wait_bounded(&empty[s], ((it / kStagesG) - 1) & 1, abort, tmo)) {
@@ -292,14 +314,13 @@ __global__ void __launch_bounds__(kThreadsG, 1)
           break;
         }
         uint8_t* row_smem = smem + kOffA + s * kABytes + (t >> 3) * 1024 + r8 * 128;
-        dequant_row_step(blk, g, row_smem, r8);
+        dequant_row_step(hdr, q0, q1, g, row_smem, r8);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(&full_w[s]);
       }
-      if (!ok) break;
     }
-  } else {
+  } else if (warp < 10) {
     // ---------------- epilogue: TMEM lanes 32*(warp%4) .. +31
     const int q = warp & 3;
     int local = 0;
@@ -325,6 +346,31 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  } else {
+    // ---------------- TMA producer (W): read once per output tile row, evict first
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      const int nsb = (int)(p.K / 256);
+      int wq = 0;
+      for (int tile = blockIdx.x; tile < total_tiles && !*abort; tile += gridDim.x) {
+        const int row0 = (tile / p.n_tiles_p) * BM;
+        for (int sb = 0; sb < nsb; ++sb, ++wq) {
+          const int w = wq % kWSlots;
+          if (wq >= kWSlots && !mbar_wait_bounded(&wempty[w], ((wq / kWSlots) - 1) & 1, abort, tmo)) {
+            if (!*abort) fail();
+            break;
+          }
+          mbar_arrive_expect_tx(&wfull[w], kWTile);
+          tma_load_2d_hint(smem + kOffW + w * kWTile, &wmap, sb * 144, row0, &wfull[w], pol);
+        }
+        if (*abort) break;
+      }
+      for (int q = wq - kWSlots < 0 ? 0 : wq - kWSlots; q < wq; ++q) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&wfull[q % kWSlots], (q / kWSlots) & 1))
+          if (globaltimer_ns() - t0 > 200000000ull) break;
+      }
     }
   }
   tc_fence_before();
@@ -406,6 +452,17 @@ extern "C" int fak_q4k_gemm(const void* Wq, int64_t N, int64_t K, const void* X,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return FAK_ERR_CUDA;
+  // W as bytes [N rows, K/256*144]: one 128-row x 144-byte box per super-block
+  CUtensorMap wmap;
+  memset(&wmap, 0, sizeof(wmap));
+  const cuuint64_t row_bytes = (cuuint64_t)(K / 256) * 144;
+  const cuuint64_t wdim[2] = {row_bytes, (cuuint64_t)N};
+  const cuuint64_t wstride[1] = {row_bytes};
+  const cuuint32_t wbox[2] = {144, BM};
+  r = g_encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(Wq), wdim, wstride, wbox, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return FAK_ERR_CUDA;
   GemmParams gp;
   gp.W = static_cast<const uint8_t*>(Wq);
   gp.Y = Y;
@@ -417,7 +474,7 @@ extern "C" int fak_q4k_gemm(const void* Wq, int64_t N, int64_t K, const void* X,
   gp.timeout_ns = 2000000000ull;
   const int tiles = gp.n_tiles_n * gp.n_tiles_p;
   const int grid = tiles < sms ? tiles : sms;
-  q4k_gemm_kernel<<<grid, kThreadsG, kSmemAllocG, (cudaStream_t)stream>>>(map, gp);
+  q4k_gemm_kernel<<<grid, kThreadsG, kSmemAllocG, (cudaStream_t)stream>>>(map, wmap, gp);
   return fak_cuda_status(cudaGetLastError());
 }
 
