@@ -37,6 +37,7 @@ constexpr int BN = 256;  // tokens per tile (MMA N)
 constexpr int BK = 64;   // K per stage (one 128-byte swizzle atom of bf16)
 constexpr int kStagesG = 3;
 constexpr int kThreadsG = 352;
+constexpr int kMaxSplits = 4;
 constexpr int kWSlots = 2;                // W super-block tiles in flight
 constexpr int kWTile = 128 * 144;       // 128 rows x 144 bytes
 constexpr int kABytes = BM * BK * 2;  // 16 KB
@@ -114,6 +115,13 @@ struct GemmParams {
   float* Y;
   int64_t N, K, P;
   int n_tiles_n, n_tiles_p;
+  // split-K: unit u is tile u / splits over super-blocks [sb_per * (u % splits), +sb_per);
+  // with splits > 1 (at most kMaxSplits) each unit leaves its partial tile in ws, row-contiguous
+  // ([tile][split][128 rows][BN tokens] f32), and per 32-row quadrant the unit that writes the
+  // last partial sums them in split order (cnt: one zeroed counter per tile quadrant)
+  int splits, sb_per;
+  float* ws;
+  unsigned* cnt;
   unsigned long long timeout_ns;
 };
 
@@ -211,7 +219,13 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   const uint32_t tmem = *tmem_slot;
 
   const int ktiles = (int)(p.K / BK);
-  const int total_tiles = p.n_tiles_n * p.n_tiles_p;
+  const int total_units = p.n_tiles_n * p.n_tiles_p * p.splits;
+  // K steps [k0, k1) of unit u
+  auto krange = [&](int u, int& k0, int& k1) {
+    const int sp = u % p.splits;
+    k0 = 4 * sp * p.sb_per;
+    k1 = min(ktiles, k0 + 4 * p.sb_per);
+  };
   const uint64_t tmo = p.timeout_ns;
   auto fail = [&]() {
     atomicCAS(&g_gemm_status, 0, FAK_ERR_TIMEOUT);
@@ -222,9 +236,12 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     // ---------------- TMA producer (X)
     if (lane == 0) {
       int it = 0;
-      for (int tile = blockIdx.x; tile < total_tiles && !*abort; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < total_units && !*abort; u += gridDim.x) {
+        const int tile = u / p.splits;
         const int p0 = (tile % p.n_tiles_p) * BN;
-        for (int kt = 0; kt < ktiles; ++kt, ++it) {
+        int k0, k1;
+        krange(u, k0, k1);
+        for (int kt = k0; kt < k1; ++kt, ++it) {
           const int s = it % kStagesG;
           if (it >= kStagesG && !mbar_wait_bounded(&empty[s], ((it / kStagesG) - 1) & 1, abort, tmo)) {
             if (!*abort) fail();
@@ -246,8 +263,10 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     // ---------------- MMA issuer
     if (lane == 0) {
       int it = 0, local = 0;
-      for (int tile = blockIdx.x; tile < total_tiles && !*abort; tile += gridDim.x, ++local) {
+      for (int u = blockIdx.x; u < total_units && !*abort; u += gridDim.x, ++local) {
         const int acc = local & 1;
+        int k0, k1;
+        krange(u, k0, k1);
         if (local >= 2 && !mbar_wait_bounded(&tempty[acc], ((local >> 1) - 1) & 1, abort, tmo)) {
           if (!*abort) fail();
           break;
@@ -255,7 +274,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         tc_fence_after();
         const uint32_t dcol = tmem + (uint32_t)(acc * BN);
         bool ok = true;
-        for (int kt = 0; kt < ktiles; ++kt, ++it) {
+        for (int kt = k0; kt < k1; ++kt, ++it) {
           const int s = it % kStagesG;
           const uint32_t ph = (it / kStagesG) & 1;
           if (!mbar_wait_bounded(&full_x[s], ph, abort, tmo) || !mbar_wait_bounded(&full_w[s], ph, abort, tmo)) {
@@ -268,7 +287,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
           const uint64_t bd = sw128_desc(smem_u32(smem + kOffB + s * kBBytes));
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            mma_bf16(dcol, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), (kt | kk) != 0);
+            mma_bf16(dcol, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), (kt != k0) || (kk != 0));
           mma_commit(&empty[s]);
         }
         if (!ok) break;
@@ -286,10 +305,12 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     const int r8 = t & 7;
     int it = 0, wq = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total_tiles && ok && !*abort; tile += gridDim.x) {
+    for (int u = blockIdx.x; u < total_units && ok && !*abort; u += gridDim.x) {
       uint4 hdr = make_uint4(0, 0, 0, 0);
       const uint8_t* rowp = nullptr;
-      for (int kt = 0; kt < ktiles && ok; ++kt, ++it) {
+      int k0, k1;
+      krange(u, k0, k1);
+      for (int kt = k0; kt < k1 && ok; ++kt, ++it) {
         const int g = kt & 3;
         if (g == 0) {
           if (!mbar_wait_bounded(&wfull[wq % kWSlots], (wq / kWSlots) & 1, abort, tmo)) {
@@ -324,8 +345,9 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     // ---------------- epilogue: TMEM lanes 32*(warp%4) .. +31
     const int q = warp & 3;
     int local = 0;
-    for (int tile = blockIdx.x; tile < total_tiles && !*abort; tile += gridDim.x, ++local) {
+    for (int u = blockIdx.x; u < total_units && !*abort; u += gridDim.x, ++local) {
       const int acc = local & 1;
+      const int tile = u / p.splits, sp = u % p.splits;
       if (!mbar_wait_bounded(&tfull[acc], (local >> 1) & 1, abort, tmo)) {
         if (!*abort) fail();
         break;
@@ -333,19 +355,72 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       tc_fence_after();
       const int64_t n = (int64_t)(tile / p.n_tiles_p) * BM + 32 * q + lane;
       const int64_t p0 = (int64_t)(tile % p.n_tiles_p) * BN;
+      // this lane's row of the partial tile (split mode)
+      float* prow = p.ws + (((int64_t)tile * p.splits + sp) * BM + 32 * q + lane) * BN;
 #pragma unroll 1
       for (int ch = 0; ch < BN / 32; ++ch) {
         uint32_t r[32];
         tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN + 32 * ch), r);
+        if (p.splits > 1) {
+          float4* d4 = reinterpret_cast<float4*>(prow + 32 * ch);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int64_t pp = p0 + 32 * ch + j;
-          if (pp < p.P) p.Y[pp * p.N + n] = __uint_as_float(r[j]);
+          for (int j = 0; j < 8; ++j)
+            d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
+                                __uint_as_float(r[4 * j + 3]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int64_t pp = p0 + 32 * ch + j;
+            if (pp < p.P) p.Y[pp * p.N + n] = __uint_as_float(r[j]);
+          }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (p.splits > 1) {
+        // per 32-row quadrant of the tile: the warp that writes the last partial sums them in
+        // split order (no barrier between warps: each quadrant has its own counter)
+        __threadfence();
+        __syncwarp();
+        unsigned prev = 0;
+        if (lane == 0) prev = atomicAdd(&p.cnt[tile * 4 + q], 1u);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == (unsigned)(p.splits - 1)) {
+          __threadfence();
+          const float* r0 = p.ws + ((int64_t)tile * p.splits * BM + 32 * q + lane) * BN;
+          const int64_t sstride = (int64_t)BM * BN;  // floats between splits of one row
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 32) {
+            float4 v[kMaxSplits][8];
+#pragma unroll
+            for (int k = 0; k < kMaxSplits; ++k)
+              if (k < p.splits) {
+                const float4* src = reinterpret_cast<const float4*>(r0 + k * sstride + c0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[k][i] = __ldcg(src + i);
+              }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float4 a = v[0][i];
+#pragma unroll
+              for (int k = 1; k < kMaxSplits; ++k)
+                if (k < p.splits) {
+                  a.x += v[k][i].x;
+                  a.y += v[k][i].y;
+                  a.z += v[k][i].z;
+                  a.w += v[k][i].w;
+                }
+              const float o[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int64_t pp = p0 + c0 + 4 * i + e;
+                if (pp < p.P) p.Y[pp * p.N + n] = o[e];
+              }
+            }
+          }
+        }
+      }
     }
   } else {
     // ---------------- TMA producer (W): read once per output tile row, evict first
@@ -353,9 +428,12 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       const uint64_t pol = l2_evict_first_policy();
       const int nsb = (int)(p.K / 256);
       int wq = 0;
-      for (int tile = blockIdx.x; tile < total_tiles && !*abort; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < total_units && !*abort; u += gridDim.x) {
+        const int tile = u / p.splits;
         const int row0 = (tile / p.n_tiles_p) * BM;
-        for (int sb = 0; sb < nsb; ++sb, ++wq) {
+        int k0, k1;
+        krange(u, k0, k1);
+        for (int sb = k0 / 4; sb < k1 / 4 && sb < nsb; ++sb, ++wq) {
           const int w = wq % kWSlots;
           if (wq >= kWSlots && !mbar_wait_bounded(&wempty[w], ((wq / kWSlots) - 1) & 1, abort, tmo)) {
             if (!*abort) fail();
@@ -473,9 +551,47 @@ extern "C" int fak_q4k_gemm(const void* Wq, int64_t N, int64_t K, const void* X,
   gp.n_tiles_p = (int)((P + BN - 1) / BN);
   gp.timeout_ns = 2000000000ull;
   const int tiles = gp.n_tiles_n * gp.n_tiles_p;
-  const int grid = tiles < sms ? tiles : sms;
-  q4k_gemm_kernel<<<grid, kThreadsG, kSmemAllocG, (cudaStream_t)stream>>>(map, wmap, gp);
-  return fak_cuda_status(cudaGetLastError());
+  const int nsb = (int)(K / 256);
+  // split-K when the tiles fill the SMs poorly: cost of s splits ~ waves(tiles*s) * (nsb/s + 12),
+  // the 12 super-blocks standing for writing and summing the partial tiles (measured)
+  int splits = 1, per = nsb;
+  double best = (double)((tiles + sms - 1) / sms) * nsb;
+  for (int sp = 2; sp <= kMaxSplits && sp <= nsb; ++sp) {
+    const int pr = (nsb + sp - 1) / sp, ns = (nsb + pr - 1) / pr;
+    const double cost = (double)((tiles * ns + sms - 1) / sms) * (pr + 12);
+    if (cost < 0.9 * best) {
+      best = cost;
+      splits = ns;
+      per = pr;
+    }
+  }
+  gp.splits = splits;
+  gp.sb_per = per;
+  gp.ws = nullptr;
+  gp.cnt = nullptr;
+  cudaStream_t s = (cudaStream_t)stream;
+  void* buf = nullptr;
+  if (splits > 1) {
+    const size_t ws_bytes = (size_t)tiles * splits * BM * BN * 4, cnt_bytes = (size_t)tiles * 4 * 4;
+    cudaError_t e = cudaMallocAsync(&buf, ws_bytes + cnt_bytes, s);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      return FAK_ERR_NOMEM;
+    }
+    gp.ws = static_cast<float*>(buf);
+    gp.cnt = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(buf) + ws_bytes);
+    e = cudaMemsetAsync(gp.cnt, 0, cnt_bytes, s);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(buf, s);
+      return fak_cuda_status(e);
+    }
+  }
+  const int units = tiles * splits;
+  const int grid = units < sms ? units : sms;
+  q4k_gemm_kernel<<<grid, kThreadsG, kSmemAllocG, s>>>(map, wmap, gp);
+  const cudaError_t le = cudaGetLastError();
+  if (buf) cudaFreeAsync(buf, s);
+  return fak_cuda_status(le);
 }
 
 int fak_gemm_take_status() {

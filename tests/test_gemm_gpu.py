@@ -42,8 +42,10 @@ def check_gemm(got, ref, a, what):
     check_f32(got, ref, a, what, rel=5e-3, abs_=1e-5, cos_min=0.9999)
 
 
+# (640, 8192, 256) and (128, 10496, 64) have few tiles: K is split across CTAs (4 splits of 8
+# super-blocks; 11 + 11 + 11 + 8) and the partial tiles are summed in split order
 @pytest.mark.parametrize("N,K,P", [(128, 256, 1), (128, 256, 7), (256, 512, 256), (384, 1280, 300),
-                                   (128, 2048, 513), (512, 5120, 64)])
+                                   (128, 2048, 513), (512, 5120, 64), (640, 8192, 256), (128, 10496, 64)])
 def test_gemm_small_full_compare(fak, N, K, P):
     w = synth.normal(40, N + K + P, (N, K), 0.02)
     Wg, Wo = fak.fak_q4k_pack(w), oracle.q4k_pack(w)
@@ -54,8 +56,8 @@ def test_gemm_small_full_compare(fak, N, K, P):
     check_gemm(Y.cpu().numpy(), Yref, A, "gemm %dx%dx%d" % (N, K, P))
 
 
-def test_gemm_deterministic(fak):
-    N, K, P = 256, 1024, 300
+@pytest.mark.parametrize("N,K,P", [(256, 1024, 300), (640, 8192, 256), (128, 10496, 64)])
+def test_gemm_deterministic(fak, N, K, P):
     w = synth.normal(42, 0, (N, K), 0.02)
     Wg = dev(fak.fak_q4k_pack(w))
     Xb = dev(synth.to_bf16(synth.normal(42, 1, (P, K), 1.0)).view(np.int16))
