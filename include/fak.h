@@ -174,7 +174,11 @@ int fak_mlp_decode_noalloc(const void* Wgate, const void* Wup, const void* Wdown
  *   Wq: device Q4_K [N x K]; X: device bf16 [P, K] row-major (bit patterns);
  *   Y: device f32 [P, N].  K % 256 == 0, N % 128 == 0, P >= 1.
  * Tensor cores (tcgen05, bf16 x bf16 -> f32): W is dequantized to bf16 in
- * shared memory, so |error| <= 5e-3 * sum|w_i x_i| + 1e-5.
+ * shared memory, so |error| <= 5e-3 * sum|w_i x_i| + 1e-5.  Deterministic.
+ * When there are too few 128 x 256 output tiles to fill the GPU, K is split
+ * across CTAs: the call then takes a stream-ordered workspace of about
+ * 128 KB per tile and split (at most 4 splits) from the device's default
+ * memory pool and frees it on the same stream; FAK_ERR_NOMEM if that fails.
  */
 int fak_q4k_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, float* Y,
                  fak_stream_t stream);
