@@ -174,6 +174,21 @@ def build_decode_model(fak, torch, n_layers=NL, vocab=V, seed=SEED_DECODE):
     return layers, lm, emb, q4_bytes + lm.numel()
 
 
+def max_over_ranks(dist, torch, x, device):
+    """The largest x over the ranks of the process group (x itself when there is no group): the job's
+    time is its slowest replica's."""
+    if dist is None:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world, ms):
+    """Whole-job tokens/s of `world` independent replicas that each decode one token per `ms`."""
+    return world * 1e3 / ms
+
+
 def time_events(torch, fn, iters):
     """Average ms per call of fn() over `iters`, CUDA events on the current stream, synchronized both sides."""
     torch.cuda.synchronize()
@@ -206,11 +221,7 @@ def bench_decode(fak, torch, args, dist, rank, world):
             ctx.step(tok, tok)
         e1.record()
         torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(dist, torch, e0.elapsed_time(e1) / args.steps, "cuda")
     st = ctx.status()
     if st != 0:
         raise RuntimeError("decode status %d" % st)
@@ -242,8 +253,10 @@ def bench_decode(fak, torch, args, dist, rank, world):
     del layers, lm, emb
     torch.cuda.empty_cache()
     algo_bytes = weight_bytes + D * 4  # + the embedding row read per token
-    return {"ms": ms, "tok_s": world * 1e3 / ms, "clocks": clk.summary(), "algo_bytes": algo_bytes,
-            "e2e_tok_s": world * 1e3 / e2e_ms, "per_matmul_ms": pm_ms, "per_matmul_launches": launches_pm}
+    e2e_ms = max_over_ranks(dist, torch, e2e_ms, "cuda")
+    return {"ms": ms, "tok_s": replica_throughput(world, ms), "clocks": clk.summary(), "algo_bytes": algo_bytes,
+            "e2e_tok_s": replica_throughput(world, e2e_ms), "per_matmul_ms": pm_ms,
+            "per_matmul_launches": launches_pm}
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
