@@ -9,26 +9,28 @@
 // where the activation stays on the GPU across every matmul of a token.
 //
 // Design (GB300-first):
-//  * One CTA per SM, 8 warps, ~216 KB shared memory.  Each warp owns a double
-//    buffer of 9 KB stages (8 rows x 8 Q4_K blocks, or 8 rows x 32 Q8_0 blocks)
-//    and streams its weight rows HBM -> shared memory with cp.async (16-byte
-//    LDGSTS, L2-only), issuing stage j+1 before computing stage j.  Weights do
-//    not depend on activations, so in a multi-step launch the next matmul's
-//    first stage is already in flight, and the following ones are prefetched
-//    into L2, while the grid waits for the previous step's output.  (Measured
-//    on GB300: per-warp LDGSTS double buffering streams at ~7.2 TB/s, while
-//    1 KB bulk copies from one issuing thread reach only ~0.5 TB/s.)
-//  * Consumers quantize x once per step into shared memory: per 256-element
+//  * One CTA per SM, 12 warps, ~227 KB shared memory.  Each warp owns three
+//    4.6 KB stage buffers (4 row slots x 8 Q4_K blocks, or 4 x 32 Q8_0 blocks)
+//    and streams its weight rows HBM -> shared memory with 16-byte cp.async
+//    (LDGSTS, L2-only), two stages in flight while it computes a third.
+//    Weights do not depend on activations, so a warp that has finished its
+//    part of a step issues the next step's third stage before the grid-wide
+//    wait.  (Measured on GB300: per-warp LDGSTS streams at ~7.2 TB/s with no
+//    compute, while 1 KB bulk copies from one issuing thread reach ~0.5 TB/s.)
+//  * Every CTA quantizes x once per step into shared memory: per 256-element
 //    super-block a power-of-two scale s with |x/s| <= 2^22, X = rint(x/s) split
 //    into three byte limbs (X = X2*65536 + X1*256 + X0, X0/X1 unsigned, X2
 //    signed).  The dot over each 32-weight sub-block is then exact integer
 //    arithmetic (DP4A on 4-bit quants x byte limbs); the sub-block scales sc_j
-//    are applied in integers, and one f32 conversion per block follows.
+//    are applied in integers, and one f32 conversion per 64 weights follows.
 //    Relative to f32 activations this adds at most 2^-23 * max|x| per element
 //    of its super-block.
-//  * Each weight row group (8 rows) is owned by one consumer warp; lanes cover
-//    (block, 64-weight group) pairs so x limbs in registers serve all 8 rows.
-//    Row results are reduced with a fixed shuffle tree: bitwise deterministic.
+//  * Lanes cover (block, 64-weight group) pairs, so the x limbs a lane holds in
+//    registers serve all four row slots of a stage.  A step's rows are cut
+//    into (4-row group, 8-block slab) units: small steps deal one CTA's units
+//    to its warps ("split"), large steps give every warp of the grid its own
+//    rows ("rows").  Row results are reduced with a fixed shuffle tree and
+//    split groups are summed in slab order: bitwise deterministic.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -314,6 +316,8 @@ __device__ __forceinline__ void prefetch_stage_l2(const Cursor& c, int lane) {
 constexpr int kMaxSbPerWarp = (kMaxSuper + kNumConsumerWarps - 1) / kNumConsumerWarps;
 constexpr int kSbBatch = 2;  // super-blocks whose loads are in flight together
 
+// x is read with L1-cached loads: in a multi-step launch they follow the
+// grid-wide acquire, so no line of an earlier step's x can be served stale.
 // One pass over x: every load is issued first, then each super-block is
 // quantized and the warp's share of sum(x^2) is left in red[cw].  The
 // RMSNorm factor is a common scale of the whole vector, so it is applied to
@@ -326,6 +330,12 @@ __device__ void prepare_x(const EngOp& op, uint8_t* smem, float* red, int cw, in
   float* xS = reinterpret_cast<float*>(smem + kOffS);
   float* xsc = reinterpret_cast<float*>(smem + kOffScale);
   float ss = 0.0f;
+  // the later batches' lines, all requested from L2 now so that their loads hit L1
+#pragma unroll
+  for (int k = kSbBatch; k < kMaxSbPerWarp; ++k) {
+    const int sb = cw + k * kNumConsumerWarps;
+    if (sb < nsb) asm volatile("prefetch.global.L1 [%0];" ::"l"(x + sb * 256 + lane * 8));
+  }
 #pragma unroll 1
   for (int k0 = 0; k0 < kMaxSbPerWarp; k0 += kSbBatch) {
   float4 va[kSbBatch], vb[kSbBatch];
@@ -334,8 +344,8 @@ __device__ void prepare_x(const EngOp& op, uint8_t* smem, float* red, int cw, in
     const int sb = cw + (k0 + k) * kNumConsumerWarps;
     if (sb < nsb) {
       const float* src = x + sb * 256 + lane * 8;
-      va[k] = ld_cg_f4(src);
-      vb[k] = ld_cg_f4(src + 4);
+      va[k] = __ldca(reinterpret_cast<const float4*>(src));
+      vb[k] = __ldca(reinterpret_cast<const float4*>(src + 4));
     }
   }
 #pragma unroll
@@ -412,15 +422,11 @@ struct XRegs {
   float SA, SB, sx16;
 };
 
-__device__ __forceinline__ void q4k_slab(const uint8_t* stage, const uint8_t* smem, int jb0, int nb, int nslots,
-                                         int lane, float acc[kSlots]) {
-  const int b = lane >> 2, g = lane & 3;
-  if (b >= nb) return;
-  const int jb = jb0 + b;
+// The x limbs of block jb, 64-weight group g, from the shared-memory records.
+__device__ __forceinline__ void load_xregs(const uint8_t* smem, int jb, int g, XRegs& x) {
   const uint8_t* rec = smem + kOffX + jb * kSuperBytes + g * kGroupRec;
   const uint4* r0 = reinterpret_cast<const uint4*>(rec);
   const uint4* r1 = reinterpret_cast<const uint4*>(rec + 96);
-  XRegs x;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint4 t;
@@ -435,25 +441,29 @@ __device__ __forceinline__ void q4k_slab(const uint8_t* stage, const uint8_t* sm
   x.SA = xS[jb * 8 + 2 * g];
   x.SB = xS[jb * 8 + 2 * g + 1];
   x.sx16 = reinterpret_cast<const float*>(smem + kOffScale)[jb] * 0.0625f;
+}
+
+// R consecutive row slots starting at `base` (a block of the first slot), one
+// 64-weight group g of that block, accumulated into acc[0..R).
+template <int R>
+__device__ __forceinline__ void q4k_rows(const uint8_t* base, int g, const XRegs& x, float (&acc)[R]) {
   const uint32_t sel = (uint32_t)(2 * g) | ((uint32_t)(2 * g + 1) << 4);
-  const uint8_t* base = stage + b * 144;
-  (void)nslots;
-  // all four row slots at once: 24 independent DP4A chains per quant word
-  uint4 h[4], qa[4], qb[4];
+  // all row slots at once: 6R independent DP4A chains per quant word
+  uint4 h[R], qa[R], qb[R];
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
+  for (int r = 0; r < R; ++r) {
     h[r] = *reinterpret_cast<const uint4*>(base + r * kQ4StageRow);
     qa[r] = *reinterpret_cast<const uint4*>(base + r * kQ4StageRow + 16 + 32 * g);
     qb[r] = *reinterpret_cast<const uint4*>(base + r * kQ4StageRow + 32 + 32 * g);
   }
-  uint32_t a0[4], a1[4], b0[4], b1[4];
-  int a2[4], b2[4];
+  uint32_t a0[R], a1[R], b0[R], b1[R];
+  int a2[R], b2[R];
 #pragma unroll
-  for (int r = 0; r < 4; ++r) a0[r] = a1[r] = b0[r] = b1[r] = 0, a2[r] = b2[r] = 0;
+  for (int r = 0; r < R; ++r) a0[r] = a1[r] = b0[r] = b1[r] = 0, a2[r] = b2[r] = 0;
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < R; ++r) {
       const uint32_t w = u < 4 ? (u == 0 ? qa[r].x : u == 1 ? qa[r].y : u == 2 ? qa[r].z : qa[r].w)
                                : (u == 4 ? qb[r].x : u == 5 ? qb[r].y : u == 6 ? qb[r].z : qb[r].w);
       const uint32_t lo = w & 0x0F0F0F0Fu, hi = w & 0xF0F0F0F0u;
@@ -466,7 +476,7 @@ __device__ __forceinline__ void q4k_slab(const uint8_t* stage, const uint8_t* sm
     }
   }
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
+  for (int r = 0; r < R; ++r) {
     const uint32_t sc_lo = h[r].y & 0x3F3F3F3Fu;
     const uint32_t m_lo = h[r].z & 0x3F3F3F3Fu;
     const uint32_t sc_hi = (h[r].w & 0x0F0F0F0Fu) | ((h[r].y >> 2) & 0x30303030u);
@@ -482,6 +492,35 @@ __device__ __forceinline__ void q4k_slab(const uint8_t* stage, const uint8_t* sm
     const float Jf = fmaf((float)J2, 65536.0f, fmaf((float)J1, 256.0f, (float)J0));
     const float mterm = fmaf(mA, x.SA, mB * x.SB);
     acc[r] = fmaf(d * x.sx16, Jf, fmaf(-dmin, mterm, acc[r]));
+  }
+}
+
+// A slab of more than four blocks: lane (b, g) = (lane/4, lane%4) takes its
+// (block, group) pair for all four row slots.  A slab of at most four blocks
+// (the last slab of a row whose length is not a multiple of eight blocks) has
+// only 16 pairs, so the upper half-warp takes row slots 2 and 3 of the same
+// pairs and each lane computes two rows: such a slab costs half a full one
+// instead of a full one with half the lanes idle.  Row slots past the valid
+// rows hold stale bytes; their sums are never written.
+__device__ __forceinline__ void q4k_slab(const uint8_t* stage, const uint8_t* smem, int jb0, int nb, int lane,
+                                         float (&acc)[kSlots]) {
+  const int g = lane & 3;
+  XRegs x;
+  if (nb > kQ4SlabBlocks / 2) {
+    const int b = lane >> 2;
+    if (b >= nb) return;
+    load_xregs(smem, jb0 + b, g, x);
+    q4k_rows<kSlots>(stage + b * 144, g, x, acc);
+  } else {
+    const int b = (lane >> 2) & 3, hr = lane >> 4;
+    if (b >= nb) return;
+    load_xregs(smem, jb0 + b, g, x);
+    float t[2] = {hr ? acc[2] : acc[0], hr ? acc[3] : acc[1]};
+    q4k_rows<2>(stage + b * 144 + 2 * hr * kQ4StageRow, g, x, t);
+    acc[0] = hr ? acc[0] : t[0];
+    acc[1] = hr ? acc[1] : t[1];
+    acc[2] = hr ? t[0] : acc[2];
+    acc[3] = hr ? t[1] : acc[3];
   }
 }
 
@@ -720,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         if (g.q8)
           q8_slab(stage, smem, s * g.slab, nb, nslots, lane, acc);
         else
-          q4k_slab(stage, smem, s * g.slab, nb, nslots, lane, acc);
+          q4k_slab(stage, smem, s * g.slab, nb, lane, acc);
         __syncwarp();
         ++j;
         if (s == g.nslab - 1 || u == pl.u1 - 1) {
