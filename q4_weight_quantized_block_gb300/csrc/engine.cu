@@ -367,25 +367,32 @@ __device__ void prepare_x(const EngOp& op, uint8_t* smem, float* red, int cw, in
       f = __uint_as_float((275u - eb) << 23);  // 2^(148-eb): |v*f| < 2^22
       sx = __uint_as_float((eb - 21u) << 23);  // 1/f
     }
-    int X[8];
-    int xsum = 0;
+    // X = rint(v * f) from one FMA: v * f is exact (f is a power of two) and
+    // |v * f| < 2^22, so v * f + 1.5 * 2^23 lands in [2^23, 2^24), where floats
+    // are the integers, rounded to nearest even once; its bits are
+    // X + 0x4B400000.  Bytes 0 and 1 of the bits are X's; byte 2 is X's signed
+    // top byte plus 64.
+    uint32_t B[8];
+    uint32_t bsum = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      X[i] = __float2int_rn(v[i] * f);
-      xsum += X[i];
+      B[i] = __float_as_uint(fmaf(v[i], f, 12582912.0f));
+      bsum += B[i];
     }
+    const int xsum_own = (int)(bsum - 8u * 0x4B400000u);  // exact: |sum X| < 2^25
     uint32_t p0[2], p1[2], p2[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      p0[h] = p1[h] = p2[h] = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int xi = X[4 * h + i];
-        p0[h] |= (uint32_t)(xi & 255) << (8 * i);
-        p1[h] |= (uint32_t)((xi >> 8) & 255) << (8 * i);
-        p2[h] |= (uint32_t)((xi >> 16) & 255) << (8 * i);
-      }
+      const uint32_t* b4 = B + 4 * h;
+      const uint32_t t01 = __byte_perm(b4[0], b4[1], 0x5140), t23 = __byte_perm(b4[2], b4[3], 0x5140);
+      p0[h] = __byte_perm(t01, t23, 0x5410);
+      p1[h] = __byte_perm(t01, t23, 0x7632);
+      const uint32_t u = __byte_perm(__byte_perm(b4[0], b4[1], 0x0062), __byte_perm(b4[2], b4[3], 0x0062), 0x5410);
+      // per byte: (X >> 16) + 64 in [0, 128) -> X >> 16 as a two's-complement byte
+      const uint32_t y = u ^ 0x40404040u;
+      p2[h] = y | ((y << 1) & 0x80808080u);
     }
+    int xsum = xsum_own;
     const int j = lane >> 2;  // sub-block
     uint8_t* rec = xq + sb * kSuperBytes + (j >> 1) * kGroupRec + (j & 1) * 96 + (lane & 3) * 8;
     *reinterpret_cast<uint2*>(rec) = make_uint2(p0[0], p0[1]);
@@ -680,6 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
   // (three copies in flight through the grid-wide wait); the next unit then skips
   // its own issue, so "wait_group 2" still means "this unit's stage has landed"
   bool ahead = false;
+  bool ahead_due = false;  // warp 0: the early issue waits for the step's release
   __syncthreads();
 
   for (int i = 0; i < P.n_ops; ++i) {
@@ -783,11 +791,15 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       }
       // the warp is done with this step's stages: the buffer of its last one is free,
       // so the next step's third stage starts loading now, before the grid-wide wait
-      if (!ahead && ic_ok && pl.u1 > pl.u0) {
+      // (warp 0 only after its thread 0 has signalled the step: the release fence
+      // waits for copies its warp has in flight)
+      ahead_due = !ahead && ic_ok && pl.u1 > pl.u0;
+      if (ahead_due && cw != 0) {
         issue_stage(ic, lane, mybuf + ((j + kBuffers - 1) % kBuffers) * kStageBytes);
         cursor_advance(P, ic, cw, lane);
         ic_ok = ic.op < P.n_ops;
         ahead = true;
+        ahead_due = false;
       }
       if (pl.split) {
         // sum each group's segments in slab order: the ends of warp runs inside the group, then the group end
@@ -843,6 +855,14 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
     // -- this CTA finished step i
     named_bar_sync(1, kConsumerThreads);
     if (ctid == 0 && P.sync) red_release_gpu_add(&P.sync[0], 1u);
+    if (ahead_due) {
+      __syncwarp();
+      issue_stage(ic, lane, mybuf + ((j + kBuffers - 1) % kBuffers) * kStageBytes);
+      cursor_advance(P, ic, cw, lane);
+      ic_ok = ic.op < P.n_ops;
+      ahead = true;
+      ahead_due = false;
+    }
   }
   // nothing may still be landing in shared memory when the CTA exits
   asm volatile("cp.async.wait_all;" ::: "memory");
