@@ -661,6 +661,12 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
   float* bestv = red + 16;                                          // [16]
   int* besti = reinterpret_cast<int*>(red + 32);                    // [16]
   volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 192);
+  // Launched as a programmatic dependent of the previous kernel on the stream
+  // (standalone matvecs): the next launch may be scheduled now, and nothing in
+  // global memory is touched before the previous grid has completed.  Both are
+  // no-ops for an ordinary or cooperative launch.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (ctid == 0) *abort = 0;
   uint8_t* mybuf = smem + kOffRing + (kBuffers * cw) * kStageBytes;
   const unsigned G = gridDim.x;
@@ -930,8 +936,20 @@ int launch_engine(const EngParams& P, int grid, bool cooperative, cudaStream_t s
     void* args[] = {const_cast<EngParams*>(&P)};
     e = cudaLaunchCooperativeKernel((const void*)engine_kernel, dim3(grid), dim3(kThreads), args, kSmemAlloc, s);
   } else {
-    engine_kernel<<<grid, kThreads, kSmemAlloc, s>>>(P);
-    e = cudaGetLastError();
+    // programmatic stream serialization: this grid's launch overlaps the end of
+    // the previous kernel, whose completion it still waits for on the device
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemAlloc;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, engine_kernel, P);
   }
   return fak_cuda_status(e);
 }
