@@ -70,6 +70,7 @@ constexpr int kOffRing = 0;
 constexpr int kOffX = kOffRing + kStages * kStageBytes;
 constexpr int kOffS = kOffX + kMaxSuper * kSuperBytes;
 constexpr int kOffScale = kOffS + kMaxSuper * 8 * 4;
+constexpr int kWarmStages = 4;                    // stages per warp warmed in L2 before a dependent launch's wait
 constexpr int kMaxUnits = 200;                    // (row group, slab) units per CTA in split mode
 constexpr int kOffPart = kOffScale + kMaxSuper * 4;
 constexpr int kOffMisc = kOffPart + kMaxUnits * kSlots * 4;
@@ -661,21 +662,32 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
   float* bestv = red + 16;                                          // [16]
   int* besti = reinterpret_cast<int*>(red + 32);                    // [16]
   volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 192);
-  // Launched as a programmatic dependent of the previous kernel on the stream
-  // (standalone matvecs): the next launch may be scheduled now, and nothing in
-  // global memory is touched before the previous grid has completed.  Both are
-  // no-ops for an ordinary or cooperative launch.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (ctid == 0) *abort = 0;
   uint8_t* mybuf = smem + kOffRing + (kBuffers * cw) * kStageBytes;
   const unsigned G = gridDim.x;
 
-  // the warp's stream of weight stages, one stage ahead of the compute
+  // the warp's stream of weight stages, one stage ahead of the compute (the
+  // step descriptors are written once by the host, never by a kernel)
   Cursor ic;
   ic.op = 0;
   cursor_load(P, ic, cw, lane);
   bool ic_ok = cursor_settle(P, ic, cw, lane);
+  // Launched as a programmatic dependent of the previous kernel on the stream
+  // (standalone and per-matmul launches), this grid may start while that
+  // kernel drains.  It lets the next launch be scheduled at once, warms L2
+  // with its first weight stages (L2 is coherent, so this is right even if the
+  // previous kernel writes the weights), and touches nothing else in global
+  // memory until the previous grid has completed.  The griddepcontrol
+  // instructions are no-ops for an ordinary or cooperative launch.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!P.sync) {
+    Cursor pc = ic;
+    for (int k = 0; k < kWarmStages && pc.op < P.n_ops; ++k) {
+      prefetch_stage_l2(pc, lane);
+      cursor_advance(P, pc, cw, lane);
+    }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // two stages in flight before the first compute; every later iteration
   // commits exactly one (possibly empty) group, so "wait_group 2" always
   // means "this iteration's stage has landed"
