@@ -130,8 +130,11 @@ int fak_q8_0_gemv(const void* Wq, int64_t N, int64_t K, const float* x, float* y
  *   fak_q4k_gemv for finite X.  Two launches (x split, then the GEMV); the
  *   call takes a stream-ordered scratch of about 4*M'*K bytes (M' = M rounded
  *   up to 8, 16, 32 or 64), plus 4*splits*M*N bytes when few row tiles force a
- *   K split, from the device's default memory pool, and frees it on the same
- *   stream.  Returns FAK_ERR_NOMEM if that allocation fails.
+ *   K split, and frees it on the same stream.  The scratch comes from a
+ *   library-owned memory pool per device that keeps its memory for later
+ *   calls until the process exits (while the stream is being captured into a
+ *   graph: cudaMallocAsync, a graph memory node).  Returns FAK_ERR_NOMEM if
+ *   that allocation fails.
  */
 int fak_q4k_gemv_batch(const void* Wq, int64_t N, int64_t K, const float* X, int M, float* Y,
                        fak_stream_t stream);
@@ -177,8 +180,10 @@ int fak_mlp_decode_noalloc(const void* Wgate, const void* Wup, const void* Wdown
  * shared memory, so |error| <= 5e-3 * sum|w_i x_i| + 1e-5.  Deterministic.
  * When there are too few 128 x 256 output tiles to fill the GPU, K is split
  * across CTAs: the call then takes a stream-ordered workspace of about
- * 128 KB per tile and split (at most 4 splits) from the device's default
- * memory pool and frees it on the same stream; FAK_ERR_NOMEM if that fails.
+ * 128 KB per tile and split (at most 4 splits) and frees it on the same
+ * stream.  It comes from the same library-owned pool as the batched GEMV's
+ * scratch (kept for later calls until the process exits; a graph memory node
+ * under stream capture); FAK_ERR_NOMEM if that fails.
  */
 int fak_q4k_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, float* Y,
                  fak_stream_t stream);

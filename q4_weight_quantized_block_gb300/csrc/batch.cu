@@ -548,7 +548,7 @@ int launch_bgemv(const uint8_t* W, int64_t N, int64_t K, const float* X, int M, 
   const size_t b_xs = up((size_t)2 * MP * K * 2), b_s = up((size_t)nsb * MP * 32), b_inv = up((size_t)nsb * MP * 4);
   const size_t b_part = splits > 1 ? up((size_t)splits * M * N * 4) : 0, b_cnt = up((size_t)tiles * 4);
   void* buf = nullptr;
-  cudaError_t e = cudaMallocAsync(&buf, b_xs + b_s + b_inv + b_part + b_cnt, s);
+  cudaError_t e = fak_scratch_alloc(&buf, b_xs + b_s + b_inv + b_part + b_cnt, s);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return FAK_ERR_NOMEM;

@@ -1006,6 +1006,39 @@ extern "C" const char* fak_strerror(int status) {
   }
 }
 
+cudaError_t fak_scratch_alloc(void** p, size_t bytes, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs != cudaStreamCaptureStatusNone) return cudaMallocAsync(p, bytes, s);
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  static std::mutex mu;
+  static cudaMemPool_t pools[64];
+  cudaMemPool_t pool;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!pools[dev]) {
+      cudaMemPoolProps props;
+      memset(&props, 0, sizeof(props));
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      e = cudaMemPoolCreate(&pools[dev], &props);
+      if (e != cudaSuccess) {
+        pools[dev] = nullptr;
+        return e;
+      }
+      uint64_t keep = ~0ull;  // never hand memory back between calls
+      cudaMemPoolSetAttribute(pools[dev], cudaMemPoolAttrReleaseThreshold, &keep);
+    }
+    pool = pools[dev];
+  }
+  return cudaMallocFromPoolAsync(p, bytes, pool, s);
+}
+
 extern "C" const char* fak_version(void) { return "fak-q4k-gb300 0.1 (sm_103a)"; }
 
 extern "C" int fak_q4k_gemv(const void* Wq, int64_t N, int64_t K, const float* x, float* y, fak_stream_t stream) {

@@ -164,3 +164,8 @@ static inline int fak_cuda_status(cudaError_t e) {
 int fak_gemm_take_status();
 // The same for the batched GEMV.
 int fak_bgemv_take_status();
+// Stream-ordered scratch for one call: from a library-owned pool per device
+// that keeps its memory for the next call (no allocation cost once warm), or,
+// while the stream is being captured into a graph, cudaMallocAsync (a graph
+// memory node).  Free with cudaFreeAsync on the same stream.
+cudaError_t fak_scratch_alloc(void** p, size_t bytes, cudaStream_t s);

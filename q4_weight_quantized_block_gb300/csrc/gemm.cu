@@ -573,7 +573,7 @@ extern "C" int fak_q4k_gemm(const void* Wq, int64_t N, int64_t K, const void* X,
   void* buf = nullptr;
   if (splits > 1) {
     const size_t ws_bytes = (size_t)tiles * splits * BM * BN * 4, cnt_bytes = (size_t)tiles * 4 * 4;
-    cudaError_t e = cudaMallocAsync(&buf, ws_bytes + cnt_bytes, s);
+    cudaError_t e = fak_scratch_alloc(&buf, ws_bytes + cnt_bytes, s);
     if (e != cudaSuccess) {
       (void)cudaGetLastError();
       return FAK_ERR_NOMEM;
