@@ -189,8 +189,11 @@ def replica_throughput(world, ms):
     return world * 1e3 / ms
 
 
-def time_events(torch, fn, iters):
-    """Average ms per call of fn() over `iters`, CUDA events on the current stream, synchronized both sides."""
+def time_events(torch, fn, iters, warmup=3):
+    """Average ms per call of fn() over `iters` after `warmup` untimed calls (lazy module loading, scratch pool
+    growth), CUDA events on the current stream, synchronized both sides."""
+    for _ in range(warmup):
+        fn()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
