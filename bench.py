@@ -437,6 +437,9 @@ def bench_components(fak, torch, hbm, bf16, which):
         synth.normal_device(Xf, 2, 2, 1.0)
         X = Xf.view(1024, D).to(torch.bfloat16)
         del scratch, Xf
+        row = D // 256 * 144
+        W13 = torch.empty_like(W1)  # gate / up rows interleaved by 16 for the fused SwiGLU epilogue
+        fak.fak_q4k_interleave_gate_up(W1[: F * row], W1[F * row:], F, D, W13)
         pre = []
         for P in (256, 512, 1024):
             Y1 = torch.empty(P * 2 * F, device="cuda")
@@ -445,11 +448,14 @@ def bench_components(fak, torch, hbm, bf16, which):
             m1 = time_events(torch, lambda: fak.fak_q4k_gemm(W1, 2 * F, D, X, P, Y1), 10)
             ms_sw = time_events(torch, lambda: fak.fak_swiglu_bf16(Y1, P, F, X2), 10)
             m2 = time_events(torch, lambda: fak.fak_q4k_gemm(W2, D, F, X2, P, Y2), 10)
+            mf = time_events(torch, lambda: fak.fak_q4k_gemm_swiglu(W13, F, D, X, P, X2), 10)
             f1, f2 = 2.0 * P * 2 * F * D, 2.0 * P * D * F
             pre.append({"P": P, "gate_up_ms": m1, "gate_up_TFLOPs": f1 / m1 / 1e9,
                         "gate_up_frac": f1 / m1 / 1e9 / bf16, "swiglu_ms": ms_sw, "down_ms": m2,
                         "down_TFLOPs": f2 / m2 / 1e9, "down_frac": f2 / m2 / 1e9 / bf16,
-                        "total_TFLOPs": (f1 + f2) / (m1 + ms_sw + m2) / 1e9})
+                        "total_TFLOPs": (f1 + f2) / (m1 + ms_sw + m2) / 1e9,
+                        "gate_up_swiglu_fused_ms": mf, "gate_up_swiglu_fused_TFLOPs": f1 / mf / 1e9,
+                        "total_fused_TFLOPs": (f1 + f2) / (mf + m2) / 1e9})
         out["prefill_gemm"] = pre
     st = fak.fak_device_status()
     if st != 0:

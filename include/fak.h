@@ -193,6 +193,33 @@ int fak_q4k_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P,
  * Y1: device f32 [P, 2*half]; X2: device bf16 [P, half]. */
 int fak_swiglu_bf16(const float* Y1, int64_t P, int64_t half, void* X2, fak_stream_t stream);
 
+/* The gate||up prefill GEMM with the SwiGLU in its epilogue (the fused form of
+ * fak_q4k_gemm then fak_swiglu_bf16; the pages' diagnosis, section 4b: the
+ * q4k_gemm prefill kernel, and the SwiGLU of the MLP in section 2):
+ *   X2[p, c] = bf16(silu(g) * u),  g = sum_k Wg[c, k] X[p, k],  u = sum_k Wu[c, k] X[p, k]
+ * without writing the f32 [P, 2F] product.
+ *   W13: device Q4_K [2F x K] in the interleaved row order written by
+ *        fak_q4k_interleave_gate_up (rows 32b..32b+15 = gate channels
+ *        16b..16b+15, rows 32b+16..32b+31 = up channels 16b..16b+15);
+ *   X: device bf16 [P, K]; X2: device bf16 [P, F], 16-byte aligned.
+ *   F % 64 == 0, K % 256 == 0, P >= 1.
+ * Each (g, u) pair is accumulated exactly as fak_q4k_gemm accumulates that row
+ * (same K order, no K split), and silu(g)*u is the expression fak_swiglu_bf16
+ * uses, so X2 equals fak_swiglu_bf16(fak_q4k_gemm(W1)) bit for bit whenever
+ * that GEMM runs without a K split (W1 = gate rows then up rows).  Scratch and
+ * errors as fak_q4k_gemm.
+ */
+int fak_q4k_gemm_swiglu(const void* W13, int64_t F, int64_t K, const void* X, int64_t P, void* X2,
+                        fak_stream_t stream);
+
+/* Writes W13 (device, 2F * K/256 * 144 bytes) from the Q4_K gate and up
+ * weights Wg, Wu (device, F * K/256 * 144 bytes each) in the row order
+ * fak_q4k_gemm_swiglu reads: a row permutation, bytes copied unchanged.
+ * F % 64 == 0, K % 256 == 0; all three pointers 16-byte aligned and W13
+ * disjoint from Wg and Wu. */
+int fak_q4k_interleave_gate_up(const void* Wg, const void* Wu, int64_t F, int64_t K, void* W13,
+                               fak_stream_t stream);
+
 /* ------------------------------------------------------------------ decode step
  * One decode token of the hybrid stack as ONE launch ([diag] section 4, the
  * "one-command-buffer-per-token GPU-resident decode forward": the activation

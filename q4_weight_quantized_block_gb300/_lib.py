@@ -57,6 +57,8 @@ _SIGS = {
     "fak_mlp_decode_noalloc": ([P, P, P, I64, I64, P, ctypes.c_float, P, P], I32),
     "fak_q4k_gemm": ([P, I64, I64, P, I64, P, P], I32),
     "fak_swiglu_bf16": ([P, I64, I64, P, P], I32),
+    "fak_q4k_gemm_swiglu": ([P, I64, I64, P, I64, P, P], I32),
+    "fak_q4k_interleave_gate_up": ([P, P, I64, I64, P, P], I32),
     "fak_decode_create": ([ctypes.POINTER(DecodeDesc), ctypes.POINTER(P)], I32),
     "fak_decode_step": ([P, P, P, P, P], I32),
     "fak_decode_status": ([P, P], I32),
@@ -172,6 +174,15 @@ def fak_q4k_gemm(Wq, N, K, X, P_, Y, stream=None):
 
 def fak_swiglu_bf16(Y1, P_, half, X2, stream=None):
     _check(lib.fak_swiglu_bf16(_ptr(Y1), P_, half, _ptr(X2), _stream(stream)), "fak_swiglu_bf16")
+
+
+def fak_q4k_gemm_swiglu(W13, F, K, X, P_, X2, stream=None):
+    _check(lib.fak_q4k_gemm_swiglu(_ptr(W13), F, K, _ptr(X), P_, _ptr(X2), _stream(stream)), "fak_q4k_gemm_swiglu")
+
+
+def fak_q4k_interleave_gate_up(Wg, Wu, F, K, W13, stream=None):
+    _check(lib.fak_q4k_interleave_gate_up(_ptr(Wg), _ptr(Wu), F, K, _ptr(W13), _stream(stream)),
+           "fak_q4k_interleave_gate_up")
 
 
 def fak_device_status(stream=None):

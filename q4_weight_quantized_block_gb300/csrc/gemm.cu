@@ -120,6 +120,11 @@ struct GemmParams {
   // ([tile][split][128 rows][BN tokens] f32), and per 32-row quadrant the unit that writes the
   // last partial sums them in split order (cnt: one zeroed counter per tile quadrant)
   int splits, sb_per;
+  // SwiGLU epilogue (fak_q4k_gemm_swiglu; splits == 1): W's rows are gate and up
+  // channels interleaved by 16 (see there); the epilogue writes
+  // x2[p, c] = bf16(silu(gate) * up) instead of Y
+  __nv_bfloat16* x2;
+  int64_t F;
   float* ws;
   unsigned* cnt;
   unsigned long long timeout_ns;
@@ -171,6 +176,9 @@ FAK_DEV void dequant_row_step(const uint4 h, const uint4 q0, const uint4 q1, int
     }
   }
 }
+
+// silu(g) * u; the one expression both SwiGLU paths use, so they agree bit for bit
+FAK_DEV float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
 __global__ void __launch_bounds__(kThreadsG, 1)
     q4k_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
@@ -361,7 +369,21 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       for (int ch = 0; ch < BN / 32; ++ch) {
         uint32_t r[32];
         tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN + 32 * ch), r);
-        if (p.splits > 1) {
+        if (p.x2) {
+          // rows 32 b + l (l < 16) are gate channel 16 b + l, rows 32 b + 16 + l its up channel:
+          // lane l < 16 finishes tokens 0..15 of this chunk and lane l + 16 tokens 16..31
+          const bool up = lane >= 16;
+          const int64_t c = (n >> 5) * 16 + (lane & 15);
+          const int64_t pb = p0 + 32 * ch + (up ? 16 : 0);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float mine = __uint_as_float(up ? r[j] : r[16 + j]);
+            const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
+            const float g = up ? other : __uint_as_float(r[j]);
+            const float u = up ? __uint_as_float(r[16 + j]) : other;
+            if (pb + j < p.P) p.x2[(pb + j) * p.F + c] = __float2bfloat16_rn(silu_mul(g, u));
+          }
+        } else if (p.splits > 1) {
           float4* d4 = reinterpret_cast<float4*>(prow + 32 * ch);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
@@ -466,7 +488,19 @@ __global__ void swiglu_bf16_kernel(const float* __restrict__ Y1, int64_t P, int6
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = i / half, c = i - r * half;
     const float g = Y1[r * 2 * half + c], u = Y1[r * 2 * half + half + c];
-    X2[i] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * u);
+    X2[i] = __float2bfloat16_rn(silu_mul(g, u));
+  }
+}
+
+// W13 row R = 32 b + l: gate row 16 b + l for l < 16, up row 16 b + l - 16 otherwise.
+__global__ void interleave_gate_up_kernel(const uint4* __restrict__ Wg, const uint4* __restrict__ Wu, int64_t F,
+                                          int64_t row16, uint4* __restrict__ W13) {
+  const int64_t total = 2 * F * row16;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t R = i / row16, k = i - R * row16;
+    const int64_t b = R >> 5, l = R & 31;
+    const int64_t src = 16 * b + (l & 15);
+    W13[i] = (l < 16 ? Wg : Wu)[src * row16 + k];
   }
 }
 
@@ -511,9 +545,9 @@ extern "C" int fak_swiglu_bf16(const float* Y1, int64_t P, int64_t half, void* X
   return fak_cuda_status(cudaGetLastError());
 }
 
-extern "C" int fak_q4k_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, float* Y,
-                            fak_stream_t stream) {
-  if (!Wq || !X || !Y) return FAK_ERR_INVALID_ARG;
+namespace {
+int launch_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, float* Y, __nv_bfloat16* x2,
+                fak_stream_t stream) {
   if (K < 256 || K % 256 || N < 128 || N % 128 || P < 1 || P > (1LL << 31) - 1 || K > (1LL << 31) - 1)
     return FAK_ERR_SHAPE;
   if ((reinterpret_cast<uintptr_t>(Wq) & 15) || (reinterpret_cast<uintptr_t>(X) & 15)) return FAK_ERR_ALIGN;
@@ -556,7 +590,7 @@ extern "C" int fak_q4k_gemm(const void* Wq, int64_t N, int64_t K, const void* X,
   // the 12 super-blocks standing for writing and summing the partial tiles (measured)
   int splits = 1, per = nsb;
   double best = (double)((tiles + sms - 1) / sms) * nsb;
-  for (int sp = 2; sp <= kMaxSplits && sp <= nsb; ++sp) {
+  for (int sp = 2; sp <= kMaxSplits && sp <= nsb && !x2; ++sp) {
     const int pr = (nsb + sp - 1) / sp, ns = (nsb + pr - 1) / pr;
     const double cost = (double)((tiles * ns + sms - 1) / sms) * (pr + 12);
     if (cost < 0.9 * best) {
@@ -567,6 +601,8 @@ extern "C" int fak_q4k_gemm(const void* Wq, int64_t N, int64_t K, const void* X,
   }
   gp.splits = splits;
   gp.sb_per = per;
+  gp.x2 = x2;
+  gp.F = N / 2;
   gp.ws = nullptr;
   gp.cnt = nullptr;
   cudaStream_t s = (cudaStream_t)stream;
@@ -592,6 +628,35 @@ extern "C" int fak_q4k_gemm(const void* Wq, int64_t N, int64_t K, const void* X,
   const cudaError_t le = cudaGetLastError();
   if (buf) cudaFreeAsync(buf, s);
   return fak_cuda_status(le);
+}
+}  // namespace
+
+extern "C" int fak_q4k_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, float* Y,
+                            fak_stream_t stream) {
+  if (!Wq || !X || !Y) return FAK_ERR_INVALID_ARG;
+  return launch_gemm(Wq, N, K, X, P, Y, nullptr, stream);
+}
+
+extern "C" int fak_q4k_gemm_swiglu(const void* W13, int64_t F, int64_t K, const void* X, int64_t P, void* X2,
+                                   fak_stream_t stream) {
+  if (!W13 || !X || !X2) return FAK_ERR_INVALID_ARG;
+  if (F < 64 || F % 64 || F > (1LL << 30)) return FAK_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(X2) & 15) return FAK_ERR_ALIGN;
+  return launch_gemm(W13, 2 * F, K, X, P, nullptr, static_cast<__nv_bfloat16*>(X2), stream);
+}
+
+extern "C" int fak_q4k_interleave_gate_up(const void* Wg, const void* Wu, int64_t F, int64_t K, void* W13,
+                                          fak_stream_t stream) {
+  if (!Wg || !Wu || !W13) return FAK_ERR_INVALID_ARG;
+  if (F < 64 || F % 64 || K < 256 || K % 256 || F > (1LL << 30) || K > (1LL << 31) - 1) return FAK_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(Wg) | reinterpret_cast<uintptr_t>(Wu) | reinterpret_cast<uintptr_t>(W13)) & 15)
+    return FAK_ERR_ALIGN;
+  const int64_t row16 = K / 256 * 144 / 16;
+  const int64_t want = (2 * F * row16 + 255) / 256;
+  const int grid = (int)(want < 152 * 32 ? want : 152 * 32);
+  interleave_gate_up_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(
+      static_cast<const uint4*>(Wg), static_cast<const uint4*>(Wu), F, row16, static_cast<uint4*>(W13));
+  return fak_cuda_status(cudaGetLastError());
 }
 
 int fak_gemm_take_status() {

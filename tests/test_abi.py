@@ -56,6 +56,14 @@ def test_validation_happens_before_any_device_call(fak):
     assert lib.fak_q4k_gemm(ok_ptr, 128, 300, ok_ptr, 8, ok_ptr, None) == 2
     assert lib.fak_q4k_gemm(ok_ptr + 8, 128, 256, ok_ptr, 8, ok_ptr, None) == 3
     assert lib.fak_q4k_gemm(None, 128, 256, ok_ptr, 8, ok_ptr, None) == 1
+    assert lib.fak_q4k_gemm_swiglu(ok_ptr, 100, 256, ok_ptr, 8, ok_ptr, None) == 2
+    assert lib.fak_q4k_gemm_swiglu(ok_ptr, 128, 300, ok_ptr, 8, ok_ptr, None) == 2
+    assert lib.fak_q4k_gemm_swiglu(ok_ptr, 128, 256, ok_ptr, 8, ok_ptr + 8, None) == 3
+    assert lib.fak_q4k_gemm_swiglu(ok_ptr, 128, 256, ok_ptr, 8, None, None) == 1
+    assert lib.fak_q4k_interleave_gate_up(ok_ptr, ok_ptr, 96, 256, ok_ptr, None) == 2
+    assert lib.fak_q4k_interleave_gate_up(ok_ptr, ok_ptr, 64, 200, ok_ptr, None) == 2
+    assert lib.fak_q4k_interleave_gate_up(ok_ptr, ok_ptr + 4, 64, 256, ok_ptr, None) == 3
+    assert lib.fak_q4k_interleave_gate_up(ok_ptr, None, 64, 256, ok_ptr, None) == 1
     assert lib.fak_decode_create(None, None) == 1
 
 

@@ -5,6 +5,12 @@ Bar: |err| <= 5e-3 * sum|w_i x_i| + 1e-5 per output and cosine >= 0.9999.
 Small shapes are compared in full; the prefill workload (fused gate||up
 34816x5120 and down 5120x17408, P = 256/512/1024 tokens, seed 2) on sampled
 rows x tokens that the oracle computes one by one.
+
+The gate||up GEMM with the SwiGLU in its epilogue is checked three ways: its
+interleaved weight rows byte for byte against the permutation written out in
+numpy, its output bit for bit against the unfused GEMM followed by the SwiGLU
+kernel (full gate||up shape, no K split), and small shapes against the oracle's
+silu(g)*u with the GEMM bar carried through the product (below).
 """
 import numpy as np
 import pytest
@@ -106,3 +112,85 @@ def test_prefill_workload_sampled(fak, P):
     rows2 = np.sort(rng.choice(D, 48, replace=False))
     Yr2, Ar2 = oracle.gemm_q4k_sample(W2o, D, F, X2h, rows2, toks)
     check_gemm(Y2.cpu().numpy()[np.ix_(toks, rows2)], Yr2, Ar2, "prefill down P=%d" % P)
+
+
+def interleave_rows(g, u):
+    """The row order fak_q4k_gemm_swiglu reads: per 16 channels, 16 gate rows then 16 up rows."""
+    F = g.shape[0]
+    out = np.empty((2 * F,) + g.shape[1:], g.dtype)
+    for b in range(F // 16):
+        out[32 * b:32 * b + 16] = g[16 * b:16 * b + 16]
+        out[32 * b + 16:32 * b + 32] = u[16 * b:16 * b + 16]
+    return out
+
+
+def test_interleave_gate_up_bytes(fak):
+    F, K = 192, 768
+    g = fak.fak_q4k_pack(synth.normal(44, 0, (F, K), 0.02))
+    u = fak.fak_q4k_pack(synth.normal(44, 1, (F, K), 0.02))
+    W13 = torch.zeros((2 * F, g.shape[1]), dtype=torch.uint8, device="cuda")
+    fak.fak_q4k_interleave_gate_up(dev(g), dev(u), F, K, W13)
+    torch.cuda.synchronize()
+    assert np.array_equal(W13.cpu().numpy(), interleave_rows(g, u))
+
+
+def bf16_bits_to_f64(t):
+    return (t.cpu().numpy().view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("P", [64, 300])
+def test_gemm_swiglu_equals_unfused(fak, P):
+    # full gate||up shape (seed 2 workload): 272 row tiles, so the unfused GEMM runs without a K split
+    D, F = 5120, 17408
+    scratch = torch.empty(2 * F * D, dtype=torch.float32, device="cuda")
+    synth.normal_device(scratch, 2, 0, 0.02)
+    W1 = torch.empty(2 * F * D // 256 * 144, dtype=torch.uint8, device="cuda")
+    fak.fak_q4k_pack_device(scratch, 2 * F, D, W1)
+    Xf = scratch[: P * D]
+    synth.normal_device(Xf, 2, 2, 1.0)
+    X = Xf.view(P, D).to(torch.bfloat16)
+    del scratch, Xf
+    row = D // 256 * 144
+    W13 = torch.empty_like(W1)
+    fak.fak_q4k_interleave_gate_up(W1[: F * row], W1[F * row:], F, D, W13)
+    Y1 = gemm(fak, W1, 2 * F, D, X, P)
+    ref = torch.empty((P, F), dtype=torch.int16, device="cuda")
+    fak.fak_swiglu_bf16(Y1, P, F, ref)
+    X2 = torch.full((P, F), -1, dtype=torch.int16, device="cuda")
+    fak.fak_q4k_gemm_swiglu(W13, F, D, X, P, X2)
+    torch.cuda.synchronize()
+    assert fak.fak_device_status() == 0
+    a, b = X2.cpu().numpy(), ref.cpu().numpy()
+    assert np.array_equal(a, b), "fused SwiGLU differs from the unfused path in %d of %d" % ((a != b).sum(), a.size)
+
+
+def silu(g):
+    return g / (1.0 + np.exp(-g))
+
+
+@pytest.mark.parametrize("F,K,P", [(64, 512, 7), (192, 1280, 300), (128, 2048, 513)])
+def test_gemm_swiglu_small_vs_oracle(fak, F, K, P):
+    # Bar: the GEMM bar per product, d = 5e-3 * sum|w x| + 1e-5 for g and for u, carried through
+    # silu(g) * u (|silu'| <= 1.1) plus one bf16 rounding (2^-8 relative) of the result.
+    wg = synth.normal(45, F + K, (F, K), 0.02)
+    wu = synth.normal(46, F + K, (F, K), 0.02)
+    Wg, Wu = oracle.q4k_pack(wg), oracle.q4k_pack(wu)
+    Xb = synth.to_bf16(synth.normal(47, F + K + P, (P, K), 1.0))
+    W13 = torch.zeros((2 * F, Wg.shape[1]), dtype=torch.uint8, device="cuda")
+    fak.fak_q4k_interleave_gate_up(dev(Wg), dev(Wu), F, K, W13)
+    X2 = torch.full((P, F), -1, dtype=torch.int16, device="cuda")
+    fak.fak_q4k_gemm_swiglu(W13, F, K, dev(Xb.view(np.int16)), P, X2)
+    torch.cuda.synchronize()
+    assert fak.fak_device_status() == 0
+    got = bf16_bits_to_f64(X2)
+    G, Ag = oracle.gemm_q4k(Wg, F, K, Xb)
+    U, Au = oracle.gemm_q4k(Wu, F, K, Xb)
+    G, U = G.astype(np.float64), U.astype(np.float64)
+    ref = silu(G) * U
+    dg, du = 5e-3 * Ag + 1e-5, 5e-3 * Au + 1e-5
+    err_in = 1.1 * np.abs(U) * dg + (np.abs(silu(G)) + 1.1 * dg) * du
+    bound = err_in + 2.0 ** -8 * (np.abs(ref) + err_in) + 1e-30
+    bad = np.abs(got - ref) > bound
+    assert not bad.any(), "swiglu gemm %dx%dx%d: %d of %d outside the bar" % (F, K, P, bad.sum(), bad.size)
+    cos = float((got * ref).sum() / np.sqrt((got * got).sum() * (ref * ref).sum()))
+    assert cos >= 0.9999, cos
