@@ -18,8 +18,9 @@
 //
 // One CTA per (128-row tile, K split), 11 warps:
 //   warp 0      TMA: W tile of one super-block, 128 rows x 144 bytes
-//   warp 1      TMA: x parts, 64-wide K chunks of [hi; lo] (128-byte swizzle),
-//               plus S and 2^-e of the super-block (bulk copies)
+//   warp 1      TMA: x parts of one super-block per ring slot, four 64-wide K
+//               chunks of [hi; lo] (128-byte swizzle), plus S and 2^-e of the
+//               super-block (bulk copies)
 //   warps 2-9   dequant sc*q to fp16 straight into TMEM (the MMA's A operand;
 //               thread = row, warp pairs split K), then the epilogue of the
 //               previous super-block (warp pairs split the input rows)
@@ -59,7 +60,8 @@ constexpr uint32_t kAccCol = 256;
 
 template <int MP>
 struct BCfg {
-  static constexpr int kSlotBytes = 2 * MP * 128;  // one 64-wide K chunk of the [hi; lo] rows
+  static constexpr int kChunkBytes = 2 * MP * 128;  // one 64-wide K chunk of the [hi; lo] rows
+  static constexpr int kSlotBytes = 4 * kChunkBytes;  // one super-block: one barrier, one commit
   static constexpr int kBStages = (kBRingBytes / kSlotBytes) > 32 ? 32 : (kBRingBytes / kSlotBytes);
   static constexpr int kSIBytes = 36 * MP;  // S [MP][8] f32, then 2^-e [MP] f32
   static constexpr int kOffB = 0;
@@ -72,7 +74,7 @@ struct BCfg {
   // kind::f16 instruction descriptor: D f32, A fp16, B fp16, both K-major, N = 2 MP, M = 128
   static constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)((2 * MP) >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
   static_assert(kSmemAlloc <= 232448, "shared memory");
-  static_assert(kSlotBytes % 1024 == 0, "swizzle atom alignment");
+  static_assert(kChunkBytes % 1024 == 0, "swizzle atom alignment");
 };
 
 struct BgParams {
@@ -264,15 +266,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       for (int i = 0; i < nloc && !*abort; ++i) {
         const int sb = sb0 + i;
         bool ok = true;
-        for (int c = 0; c < 4; ++c) {
-          const int qq = 4 * i + c, slot = qq % C::kBStages;
-          if (qq >= C::kBStages && !mbar_wait_bounded(&bempty[slot], ((qq / C::kBStages) - 1) & 1, abort, tmo)) {
-            ok = false;
-            break;
-          }
+        const int slot = i % C::kBStages;
+        if (i >= C::kBStages && !mbar_wait_bounded(&bempty[slot], ((i / C::kBStages) - 1) & 1, abort, tmo)) ok = false;
+        if (ok) {
           mbar_arrive_expect_tx(&bfull[slot], C::kSlotBytes);
-          tma_load_2d_tx(smem + C::kOffB + slot * C::kSlotBytes, &xmap, sb * 256 + 64 * c, 0, &bfull[slot]);
-          issued_b = qq + 1;
+          for (int c = 0; c < 4; ++c)
+            tma_load_2d_tx(smem + C::kOffB + slot * C::kSlotBytes + c * C::kChunkBytes, &xmap, sb * 256 + 64 * c, 0,
+                           &bfull[slot]);
+          issued_b = i + 1;
         }
         const int s = i % kSIStages;
         if (ok && i >= kSIStages && !mbar_wait_bounded(&sempty[s], ((i / kSIStages) - 1) & 1, abort, tmo)) ok = false;
@@ -310,19 +311,19 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem + kAccCol + 128u * (uint32_t)a;
         const uint32_t a_tmem = tmem + 128u * (uint32_t)a;
-        bool ok = true;
-        for (int c = 0; c < 4; ++c) {
-          const int qq = 4 * i + c, slot = qq % C::kBStages;
-          if (!mbar_wait_bounded(&bfull[slot], (qq / C::kBStages) & 1, abort, tmo)) {
-            ok = false;
-            break;
-          }
+        const int slot = i % C::kBStages;
+        const bool ok = mbar_wait_bounded(&bfull[slot], (i / C::kBStages) & 1, abort, tmo);
+        if (ok) {
           tc_fence_after_sync();
-          const uint64_t bdesc = umma_desc_sw128(smem_u32(smem + C::kOffB + slot * C::kSlotBytes));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_f16_ts(d_tmem, a_tmem + (uint32_t)(32 * c + 8 * kk), bdesc + (uint64_t)(2 * kk), C::kIdesc,
-                        (c | kk) != 0);
+          for (int c = 0; c < 4; ++c) {
+            const uint64_t bdesc =
+                umma_desc_sw128(smem_u32(smem + C::kOffB + slot * C::kSlotBytes + c * C::kChunkBytes));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_f16_ts(d_tmem, a_tmem + (uint32_t)(32 * c + 8 * kk), bdesc + (uint64_t)(2 * kk), C::kIdesc,
+                          (c | kk) != 0);
+          }
           umma_commit(&bempty[slot]);
         }
         if (!ok) {
