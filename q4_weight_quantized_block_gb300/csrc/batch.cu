@@ -180,8 +180,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   uint64_t* sfull = bempty + C::kBStages;
   uint64_t* sempty = sfull + kSIStages;
   uint64_t* afull = sempty + kSIStages;
-  uint64_t* aempty = afull + 2;
-  uint64_t* cfull = aempty + 2;
+  // cfull[a]: the MMAs of the super-block in buffer pair a are done, so its
+  // accumulator is ready for the epilogue and its A buffer free for the dequant
+  uint64_t* cfull = afull + 2;
   uint64_t* cempty = cfull + 2;
   uint64_t* drain = cempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -208,7 +209,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&afull[a], 8);
-      mbar_init(&aempty[a], 1);
       mbar_init(&cfull[a], 1);
       mbar_init(&cempty[a], 8);
     }
@@ -330,7 +330,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           if (!*abort) fail();
           break;
         }
-        umma_commit(&aempty[a]);
         umma_commit(&cfull[a]);
       }
       umma_commit(drain);
@@ -414,7 +413,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
       // scales of this thread's four sub-blocks 4hh .. 4hh+3
       const uint32_t scw = hh ? ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u)) : (hdr.y & 0x3F3F3F3Fu);
-      if (i >= 2 && !mbar_wait_bounded(&aempty[i & 1], ((i >> 1) - 1) & 1, abort, tmo)) {
+      if (i >= 2 && !mbar_wait_bounded(&cfull[i & 1], ((i >> 1) - 1) & 1, abort, tmo)) {
         ok = false;
         break;
       }
