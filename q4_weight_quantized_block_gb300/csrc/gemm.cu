@@ -6,7 +6,7 @@
 // mlp_down_proj take 73% of prefill; section 4b: the q4k_gemm prefill kernel).
 //
 // One CTA per SM, persistent over output tiles of 128 weight rows x 256 tokens,
-// K in steps of 64 through a 4-stage shared-memory pipeline:
+// K in steps of 64 through a 3-stage shared-memory pipeline:
 //   warp 0      TMA producer: X tile [256 tokens x 64] bf16, 128-byte swizzle
 //   warp 1      TMEM owner + MMA issuer: 4 x tcgen05.mma (M128 N256 K16) per stage
 //   warps 2-5   dequant producers: 128 W rows x 64 weights -> bf16, written in the

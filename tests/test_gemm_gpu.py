@@ -194,3 +194,29 @@ def test_gemm_swiglu_small_vs_oracle(fak, F, K, P):
     assert not bad.any(), "swiglu gemm %dx%dx%d: %d of %d outside the bar" % (F, K, P, bad.sum(), bad.size)
     cos = float((got * ref).sum() / np.sqrt((got * got).sum() * (ref * ref).sum()))
     assert cos >= 0.9999, cos
+
+
+def test_gemm_and_batch_under_graph_capture(fak):
+    # while a stream is being captured their scratch comes from cudaMallocAsync (a graph memory
+    # node), otherwise from the library's pool: replays equal the eager results bit for bit
+    N, K, P, M = 640, 8192, 256, 8  # the GEMM takes a K split here, so it has a workspace
+    Wg = dev(fak.fak_q4k_pack(synth.normal(48, 0, (N, K), 0.02)))
+    Xb = dev(synth.to_bf16(synth.normal(48, 1, (P, K), 1.0)).view(np.int16))
+    Xf = dev(synth.normal(48, 2, (M, K), 1.0))
+    Y_e, Yb_e = torch.empty((P, N), device="cuda"), torch.empty((M, N), device="cuda")
+    fak.fak_q4k_gemm(Wg, N, K, Xb, P, Y_e)
+    fak.fak_q4k_gemv_batch(Wg, N, K, Xf, M, Yb_e)
+    torch.cuda.synchronize()
+    Y_g, Yb_g = torch.full((P, N), float("nan"), device="cuda"), torch.full((M, N), float("nan"), device="cuda")
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            fak.fak_q4k_gemm(Wg, N, K, Xb, P, Y_g)
+            fak.fak_q4k_gemv_batch(Wg, N, K, Xf, M, Yb_g)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert fak.fak_device_status() == 0
+    assert np.array_equal(Y_g.cpu().numpy().view(np.uint32), Y_e.cpu().numpy().view(np.uint32))
+    assert np.array_equal(Yb_g.cpu().numpy().view(np.uint32), Yb_e.cpu().numpy().view(np.uint32))
