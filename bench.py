@@ -252,6 +252,23 @@ def bench_decode(fak, torch, args, dist, rank, world):
     pm_ms = time_events(torch, lambda: ctx_pm.step(tok, tok), max(3, args.steps // 3))
     launches_pm = ctx_pm.launches_per_step()
     ctx_pm.close()
+
+    # the int8-activation variant of the same step (Q4_K steps on int8 x), and how far its logits
+    # move from the exact step's on one token
+    ctx_i8 = fak.DecodeContext(D, F, args.vocab, GI, QG, KV, NM, layers, lm, emb, mode=fak.FAK_DECODE_ONE_LAUNCH_I8X)
+    i8_ms = time_events(torch, lambda: ctx_i8.step(tok, tok), max(3, args.steps // 3))
+    t0_tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    le, li = torch.empty(args.vocab, device="cuda"), torch.empty(args.vocab, device="cuda")
+    o1, o2 = torch.zeros(1, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+    ctx.step(t0_tok, o1, le)
+    ctx_i8.step(t0_tok, o2, li)
+    st = ctx_i8.status()
+    if st != 0:
+        raise RuntimeError("int8 decode status %d" % st)
+    le64, li64 = le.double(), li.double()
+    i8_cos = float((le64 * li64).sum() / torch.sqrt((le64 * le64).sum() * (li64 * li64).sum()))
+    i8_same_tok = int(o1.item()) == int(o2.item())
+    ctx_i8.close()
     ctx.close()
     del layers, lm, emb
     torch.cuda.empty_cache()
@@ -259,7 +276,8 @@ def bench_decode(fak, torch, args, dist, rank, world):
     e2e_ms = max_over_ranks(dist, torch, e2e_ms, "cuda")
     return {"ms": ms, "tok_s": replica_throughput(world, ms), "clocks": clk.summary(), "algo_bytes": algo_bytes,
             "e2e_tok_s": replica_throughput(world, e2e_ms), "per_matmul_ms": pm_ms,
-            "per_matmul_launches": launches_pm}
+            "per_matmul_launches": launches_pm, "i8x_ms": i8_ms, "i8x_logits_cosine": i8_cos,
+            "i8x_same_token": i8_same_tok}
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
@@ -373,11 +391,18 @@ def bench_components(fak, torch, hbm, bf16, which):
             def one():
                 fak.fak_q4k_gemv(Ws[it[0] % copies], N, K, x, y)
                 it[0] += 1
-            us = graph_time(torch, one, max(copies, 20) if copies > 1 else 5)
+
+            def one_i8():
+                fak.fak_q4k_gemv_i8x(Ws[it[0] % copies], N, K, x, y)
+                it[0] += 1
+            reps = max(copies, 20) if copies > 1 else 5
+            us = graph_time(torch, one, reps)
             ue = time_events(torch, one, 50 if N * K < 100_000_000 else 10) * 1e3
+            us8 = graph_time(torch, one_i8, reps)
             byts = N * K // 256 * 144 + 4 * (N + K)
             return {"N": N, "K": K, "us": us, "GBps": byts / us / 1e3, "frac": byts / us / 1e3 / hbm,
-                    "us_eager": ue, "rotating_copies": copies, "bytes": byts}
+                    "us_eager": ue, "rotating_copies": copies, "bytes": byts,
+                    "int8_activations": {"us": us8, "GBps": byts / us8 / 1e3, "frac": byts / us8 / 1e3 / hbm}}
 
         # single GEMV 5120 x 5120 (seed 0: W tensor 0, x tensor 1)
         out["gemv_5120x5120"] = gemv_case(5120, 5120, 0, 0, 1)
@@ -525,6 +550,10 @@ def main():
         "gpu_launches": args.steps,
         "per_matmul_mode": {"ms_per_step": dec["per_matmul_ms"], "tok_s": 1e3 / dec["per_matmul_ms"],
                             "launches_per_step": dec["per_matmul_launches"]},
+        "int8_activation_variant": {"ms_per_step": dec["i8x_ms"], "tok_s": 1e3 / dec["i8x_ms"],
+                                    "roofline_frac": dec["algo_bytes"] / (dec["i8x_ms"] * 1e-3) / 1e9 / hbm,
+                                    "logits_cosine_vs_exact": dec["i8x_logits_cosine"],
+                                    "same_token_as_exact": dec["i8x_same_token"]},
         "components": comps,
     }
     print(json.dumps(line))

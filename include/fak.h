@@ -113,6 +113,17 @@ int fak_q8_0_pack_device(const float* w, int64_t N, int64_t K, void* out, size_t
  */
 int fak_q4k_gemv(const void* Wq, int64_t N, int64_t K, const float* x, float* y, fak_stream_t stream);
 
+/* The int8-activation variant of fak_q4k_gemv ([parity] reconciliation table:
+ * the int8-SDOT Metal decode GEMV path, checked by cosine).  Each 32-element
+ * sub-block of x becomes d_j * X_k with d_j = max|x| / 127 and
+ * X_k = rint(x_k * (127 / max|x|)) in [-127, 127] (f32 arithmetic, ties to
+ * even); y is then the f32-accumulate dot of W with that quantized x, exact
+ * per sub-block in integers, so it meets 1e-5 * sum|w_i x~_i| + 1e-6 against
+ * the quantized activations x~ -- not against x: the quantization itself
+ * moves each element by up to max|x| / 254 of its sub-block.  One third of
+ * the integer work of fak_q4k_gemv.  Same arguments, limits and determinism. */
+int fak_q4k_gemv_i8x(const void* Wq, int64_t N, int64_t K, const float* x, float* y, fak_stream_t stream);
+
 /* Same for a Q8_0 matrix (the lm_head format of [diag] section 2, lm_head_q8).
  * K % 256 == 0 (so rows stay 16-byte aligned), K <= FAK_ENGINE_MAX_K. */
 int fak_q8_0_gemv(const void* Wq, int64_t N, int64_t K, const float* x, float* y, fak_stream_t stream);
@@ -234,7 +245,11 @@ int fak_q4k_interleave_gate_up(const void* Wg, const void* Wu, int64_t F, int64_
  *   index on ties.  RMSNorm gain is 1.
  */
 enum { FAK_LAYER_GDN = 0, FAK_LAYER_FA = 1 };
-enum { FAK_DECODE_ONE_LAUNCH = 0, FAK_DECODE_PER_MATMUL = 1 };
+/* ONE_LAUNCH: the whole token is one cooperative launch; PER_MATMUL: one launch
+ * per step.  The _I8X modes are the same launch shapes with every Q4_K step on
+ * int8 activations (fak_q4k_gemv_i8x); the Q8_0 lm_head keeps the exact form. */
+enum { FAK_DECODE_ONE_LAUNCH = 0, FAK_DECODE_PER_MATMUL = 1, FAK_DECODE_ONE_LAUNCH_I8X = 2,
+       FAK_DECODE_PER_MATMUL_I8X = 3 };
 
 typedef struct {
     int32_t kind;          /* FAK_LAYER_GDN or FAK_LAYER_FA */
@@ -252,7 +267,7 @@ typedef struct {
     int32_t d_model, d_ff, vocab;
     int32_t gdn_in, fa_qg, fa_kv, n_mix;
     float eps;
-    int32_t mode;                 /* FAK_DECODE_ONE_LAUNCH or FAK_DECODE_PER_MATMUL */
+    int32_t mode;                 /* FAK_DECODE_ONE_LAUNCH, _PER_MATMUL, _ONE_LAUNCH_I8X or _PER_MATMUL_I8X */
     const fak_layer_desc* layers; /* host array of n_layers; copied by fak_decode_create */
     const void* lm_head;          /* [vocab x d_model] Q8_0, device */
     const float* embedding;       /* [vocab x d_model] f32, device */

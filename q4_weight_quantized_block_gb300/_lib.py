@@ -18,7 +18,7 @@ STATUS = {0: "FAK_OK", 1: "FAK_ERR_INVALID_ARG", 2: "FAK_ERR_SHAPE", 3: "FAK_ERR
 FAK_ENGINE_MAX_K = 18432
 FAK_MLP_NOALLOC_MAX_FF = 18432
 FAK_LAYER_GDN, FAK_LAYER_FA = 0, 1
-FAK_DECODE_ONE_LAUNCH, FAK_DECODE_PER_MATMUL = 0, 1
+FAK_DECODE_ONE_LAUNCH, FAK_DECODE_PER_MATMUL, FAK_DECODE_ONE_LAUNCH_I8X, FAK_DECODE_PER_MATMUL_I8X = 0, 1, 2, 3
 
 P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
 
@@ -50,6 +50,7 @@ _SIGS = {
     "fak_q4k_pack_device": ([P, I64, I64, P, SZ, P], I32),
     "fak_q8_0_pack_device": ([P, I64, I64, P, SZ, P], I32),
     "fak_q4k_gemv": ([P, I64, I64, P, P, P], I32),
+    "fak_q4k_gemv_i8x": ([P, I64, I64, P, P, P], I32),
     "fak_q8_0_gemv": ([P, I64, I64, P, P, P], I32),
     "fak_q4k_gemv_batch": ([P, I64, I64, P, I32, P, P], I32),
     "fak_mlp_workspace_bytes": ([I64], SZ),
@@ -141,6 +142,11 @@ def fak_q8_0_pack_device(w, N, K, out, stream=None):
 # ------------------------------------------------------------------ device calls
 def fak_q4k_gemv(Wq, N, K, x, y, stream=None):
     _check(lib.fak_q4k_gemv(_ptr(Wq), N, K, _ptr(x), _ptr(y), _stream(stream)), "fak_q4k_gemv")
+
+
+def fak_q4k_gemv_i8x(Wq, N, K, x, y, stream=None):
+    """fak_q4k_gemv on int8 activations (one scale per 32-element sub-block of x)."""
+    _check(lib.fak_q4k_gemv_i8x(_ptr(Wq), N, K, _ptr(x), _ptr(y), _stream(stream)), "fak_q4k_gemv_i8x")
 
 
 def fak_q8_0_gemv(Wq, N, K, x, y, stream=None):

@@ -324,7 +324,10 @@ constexpr int kSbBatch = 2;  // super-blocks whose loads are in flight together
 // RMSNorm factor is a common scale of the whole vector, so it is applied to
 // the row results in the epilogue instead (the per-super-block power-of-two
 // scales keep the same relative precision either way).
+template <bool I8>
 __device__ void prepare_x(const EngOp& op, uint8_t* smem, float* red, int cw, int lane) {
+  // int8 activations (the variant of the pages' int8-SDOT decode GEMV) for Q4_K steps only
+  const bool i8 = I8 && op.kind != OP_Q8;
   const float* x = op.x;
   const int nsb = op.K / 256;
   uint8_t* xq = smem + kOffX;
@@ -354,6 +357,38 @@ __device__ void prepare_x(const EngOp& op, uint8_t* smem, float* red, int cw, in
     const int sb = cw + (k0 + k) * kNumConsumerWarps;
     if (sb >= nsb) break;
     const float v[8] = {va[k].x, va[k].y, va[k].z, va[k].w, vb[k].x, vb[k].y, vb[k].z, vb[k].w};
+    if (i8) {
+      // per 32-element sub-block (four lanes): d = max|x| / 127, X = rint(x * (127 / max|x|)),
+      // one signed byte each; the dot then sums q * X exactly and scales by d
+      float am8 = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        am8 = fmaxf(am8, fabsf(v[i]));
+        ss = fmaf(v[i], v[i], ss);
+      }
+      am8 = fmaxf(am8, __shfl_xor_sync(0xffffffffu, am8, 1));
+      am8 = fmaxf(am8, __shfl_xor_sync(0xffffffffu, am8, 2));
+      const float qs = am8 > 0.0f ? 127.0f / am8 : 0.0f;
+      const float dsub = am8 / 127.0f;
+      int Xi[8], xs = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        Xi[i] = max(-127, min(127, __float2int_rn(v[i] * qs)));
+        xs += Xi[i];
+      }
+      const uint32_t w0 = __byte_perm(__byte_perm(Xi[0], Xi[1], 0x0040), __byte_perm(Xi[2], Xi[3], 0x0040), 0x5410);
+      const uint32_t w1 = __byte_perm(__byte_perm(Xi[4], Xi[5], 0x0040), __byte_perm(Xi[6], Xi[7], 0x0040), 0x5410);
+      const int j = lane >> 2;  // sub-block
+      uint8_t* grec = xq + sb * kSuperBytes + (j >> 1) * kGroupRec;
+      *reinterpret_cast<uint2*>(grec + (j & 1) * 96 + (lane & 3) * 8) = make_uint2(w0, w1);
+      xs += __shfl_xor_sync(0xffffffffu, xs, 1);
+      xs += __shfl_xor_sync(0xffffffffu, xs, 2);
+      if ((lane & 3) == 0) {
+        reinterpret_cast<float*>(grec + 32)[j & 1] = dsub;  // the second limb's slot is free here
+        xS[sb * 8 + j] = dsub * (float)xs;
+      }
+      continue;
+    }
     float am = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -500,6 +535,93 @@ __device__ __forceinline__ void q4k_rows(const uint8_t* base, int g, const XRegs
     const float Jf = fmaf((float)J2, 65536.0f, fmaf((float)J1, 256.0f, (float)J0));
     const float mterm = fmaf(mA, x.SA, mB * x.SB);
     acc[r] = fmaf(d * x.sx16, Jf, fmaf(-dmin, mterm, acc[r]));
+  }
+}
+
+// int8-activation form: the x bytes of sub-blocks 2g and 2g+1, their scales and sums.
+struct XRegs8 {
+  uint32_t A[8], B[8];
+  float dA, dB, SA, SB;
+};
+
+__device__ __forceinline__ void load_xregs8(const uint8_t* smem, int jb, int g, XRegs8& x) {
+  const uint8_t* rec = smem + kOffX + jb * kSuperBytes + g * kGroupRec;
+  const uint4* r0 = reinterpret_cast<const uint4*>(rec);
+  const uint4* r1 = reinterpret_cast<const uint4*>(rec + 96);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint4 t = r0[h];
+    x.A[4 * h] = t.x; x.A[4 * h + 1] = t.y; x.A[4 * h + 2] = t.z; x.A[4 * h + 3] = t.w;
+    t = r1[h];
+    x.B[4 * h] = t.x; x.B[4 * h + 1] = t.y; x.B[4 * h + 2] = t.z; x.B[4 * h + 3] = t.w;
+  }
+  const float2 dd = *reinterpret_cast<const float2*>(rec + 32);
+  x.dA = dd.x;
+  x.dB = dd.y;
+  const float* xS = reinterpret_cast<const float*>(smem + kOffS);
+  x.SA = xS[jb * 8 + 2 * g];
+  x.SB = xS[jb * 8 + 2 * g + 1];
+}
+
+template <int R>
+__device__ __forceinline__ void q4k_rows8(const uint8_t* base, int g, const XRegs8& x, float (&acc)[R]) {
+  const uint32_t sel = (uint32_t)(2 * g) | ((uint32_t)(2 * g + 1) << 4);
+  uint4 h[R], qa[R], qb[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    h[r] = *reinterpret_cast<const uint4*>(base + r * kQ4StageRow);
+    qa[r] = *reinterpret_cast<const uint4*>(base + r * kQ4StageRow + 16 + 32 * g);
+    qb[r] = *reinterpret_cast<const uint4*>(base + r * kQ4StageRow + 32 + 32 * g);
+  }
+  int a[R], b[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) a[r] = b[r] = 0;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const uint32_t w = u < 4 ? (u == 0 ? qa[r].x : u == 1 ? qa[r].y : u == 2 ? qa[r].z : qa[r].w)
+                               : (u == 4 ? qb[r].x : u == 5 ? qb[r].y : u == 6 ? qb[r].z : qb[r].w);
+      a[r] = dp4a_us(w & 0x0F0F0F0Fu, x.A[u], a[r]);
+      b[r] = dp4a_us(w & 0xF0F0F0F0u, x.B[u], b[r]);  // 16 q: the scale below divides by 16
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const uint32_t sc_lo = h[r].y & 0x3F3F3F3Fu;
+    const uint32_t m_lo = h[r].z & 0x3F3F3F3Fu;
+    const uint32_t sc_hi = (h[r].w & 0x0F0F0F0Fu) | ((h[r].y >> 2) & 0x30303030u);
+    const uint32_t m_hi = ((h[r].w >> 4) & 0x0F0F0F0Fu) | ((h[r].z >> 2) & 0x30303030u);
+    const uint32_t scp = prmt(sc_lo, sc_hi, sel);
+    const uint32_t mp = prmt(m_lo, m_hi, sel);
+    const int scA16 = (int)(scp & 0xFF) << 4, scB = (int)((scp >> 8) & 0xFF);
+    const float mA = (float)(mp & 0xFF), mB = (float)((mp >> 8) & 0xFF);
+    const float d = half_bits_to_float(h[r].x & 0xFFFF), dmin = half_bits_to_float(h[r].x >> 16);
+    const float Jf = fmaf((float)(a[r] * scA16), x.dA, (float)(b[r] * scB) * x.dB);
+    const float mterm = fmaf(mA, x.SA, mB * x.SB);
+    acc[r] = fmaf(d * 0.0625f, Jf, fmaf(-dmin, mterm, acc[r]));
+  }
+}
+
+__device__ __forceinline__ void q4k_slab8(const uint8_t* stage, const uint8_t* smem, int jb0, int nb, int lane,
+                                          float (&acc)[kSlots]) {
+  const int g = lane & 3;
+  XRegs8 x;
+  if (nb > kQ4SlabBlocks / 2) {
+    const int b = lane >> 2;
+    if (b >= nb) return;
+    load_xregs8(smem, jb0 + b, g, x);
+    q4k_rows8<kSlots>(stage + b * 144, g, x, acc);
+  } else {
+    const int b = (lane >> 2) & 3, hr = lane >> 4;
+    if (b >= nb) return;
+    load_xregs8(smem, jb0 + b, g, x);
+    float t[2] = {hr ? acc[2] : acc[0], hr ? acc[3] : acc[1]};
+    q4k_rows8<2>(stage + b * 144 + 2 * hr * kQ4StageRow, g, x, t);
+    acc[0] = hr ? acc[0] : t[0];
+    acc[1] = hr ? acc[1] : t[1];
+    acc[2] = hr ? t[0] : acc[2];
+    acc[3] = hr ? t[1] : acc[3];
   }
 }
 
@@ -653,6 +775,9 @@ __device__ __forceinline__ float reduce4(const float (&acc)[kSlots], int lane) {
 }
 
 // ------------------------------------------------------------------ the steps
+// I8X: Q4_K steps take int8 activations (one scale per 32-element sub-block)
+// instead of the exact three-limb form; Q8_0 steps are the same in both.
+template <bool I8X>
 __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_constant__ EngParams P) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -751,7 +876,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         if (lane == 0 && P.tok_out) *P.tok_out = bi < 0 ? 0 : bi;
       }
     } else {
-      prepare_x(op, smem, red, cw, lane);
+      prepare_x<I8X>(op, smem, red, cw, lane);
       named_bar_sync(1, kConsumerThreads);
       const float rn = norm_factor(op, red);
       const Geo g = geo_of(op);
@@ -784,6 +909,8 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         const int nb = min(g.slab, g.bpr - s * g.slab);
         if (g.q8)
           q8_slab(stage, smem, s * g.slab, nb, nslots, lane, acc);
+        else if (I8X)
+          q4k_slab8(stage, smem, s * g.slab, nb, lane, acc);
         else
           q4k_slab(stage, smem, s * g.slab, nb, lane, acc);
         __syncwarp();
@@ -915,7 +1042,9 @@ int device_setup(int* sms) {
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
     if (major != 10 || minor != 3) return FAK_ERR_UNSUPPORTED;
-    cudaError_t e = cudaFuncSetAttribute(engine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    cudaError_t e = cudaFuncSetAttribute(engine_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (e != cudaSuccess) return fak_cuda_status(e);
+    e = cudaFuncSetAttribute(engine_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return fak_cuda_status(e);
     di.attr_set = true;
     di.ok = true;
@@ -942,11 +1071,12 @@ EngOp make_matvec(int kind, const void* W, int64_t N, int64_t K, const float* x,
   return op;
 }
 
-int launch_engine(const EngParams& P, int grid, bool cooperative, cudaStream_t s) {
+int launch_engine(const EngParams& P, int grid, bool cooperative, cudaStream_t s, bool i8x = false) {
+  void (*kern)(EngParams) = i8x ? engine_kernel<true> : engine_kernel<false>;
   cudaError_t e;
   if (cooperative) {
     void* args[] = {const_cast<EngParams*>(&P)};
-    e = cudaLaunchCooperativeKernel((const void*)engine_kernel, dim3(grid), dim3(kThreads), args, kSmemAlloc, s);
+    e = cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(kThreads), args, kSmemAlloc, s);
   } else {
     // programmatic stream serialization: this grid's launch overlaps the end of
     // the previous kernel, whose completion it still waits for on the device
@@ -961,7 +1091,7 @@ int launch_engine(const EngParams& P, int grid, bool cooperative, cudaStream_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, engine_kernel, P);
+    e = cudaLaunchKernelEx(&cfg, kern, P);
   }
   return fak_cuda_status(e);
 }
@@ -973,7 +1103,8 @@ EngParams base_params() {
   return P;
 }
 
-int single_matvec(int kind, const void* W, int64_t N, int64_t K, const float* x, float* y, cudaStream_t s) {
+int single_matvec(int kind, const void* W, int64_t N, int64_t K, const float* x, float* y, cudaStream_t s,
+                  bool i8x = false) {
   if (!W || !x || !y) return FAK_ERR_INVALID_ARG;
   if (N < 1 || N > 0x7fffffffLL || K < 256 || K % 256 != 0 || K > FAK_ENGINE_MAX_K) return FAK_ERR_SHAPE;
   if (!aligned16(W) || !aligned16(x)) return FAK_ERR_ALIGN;
@@ -985,7 +1116,7 @@ int single_matvec(int kind, const void* W, int64_t N, int64_t K, const float* x,
   P.n_ops = 1;
   const int64_t groups = (N + kRowsPerGroup - 1) / kRowsPerGroup;
   const int grid = (int)std::min<int64_t>(groups, sms);
-  return launch_engine(P, grid, false, s);
+  return launch_engine(P, grid, false, s, i8x);
 }
 
 }  // namespace
@@ -1043,6 +1174,11 @@ extern "C" const char* fak_version(void) { return "fak-q4k-gb300 0.1 (sm_103a)";
 
 extern "C" int fak_q4k_gemv(const void* Wq, int64_t N, int64_t K, const float* x, float* y, fak_stream_t stream) {
   return single_matvec(OP_Q4K, Wq, N, K, x, y, (cudaStream_t)stream);
+}
+
+extern "C" int fak_q4k_gemv_i8x(const void* Wq, int64_t N, int64_t K, const float* x, float* y,
+                                fak_stream_t stream) {
+  return single_matvec(OP_Q4K, Wq, N, K, x, y, (cudaStream_t)stream, true);
 }
 
 extern "C" int fak_q8_0_gemv(const void* Wq, int64_t N, int64_t K, const float* x, float* y, fak_stream_t stream) {
@@ -1159,7 +1295,8 @@ struct fak_decode {
   fak_decode_desc desc;
   std::vector<fak_layer_desc> layers;
   int sms = 0;
-  int mode = 0;
+  int mode = 0;    // FAK_DECODE_ONE_LAUNCH or FAK_DECODE_PER_MATMUL
+  bool i8x = false;  // int8 activations for the Q4_K steps
   int n_ops = 0;
   int n_fa = 0;
   EngOp* d_ops = nullptr;
@@ -1202,7 +1339,7 @@ int upload_ops(fak_decode* c) {
 extern "C" int fak_decode_create(const fak_decode_desc* d, fak_decode** out) {
   if (!d || !out || !d->layers || !d->lm_head || !d->embedding) return FAK_ERR_INVALID_ARG;
   *out = nullptr;
-  if (d->mode != FAK_DECODE_ONE_LAUNCH && d->mode != FAK_DECODE_PER_MATMUL) return FAK_ERR_INVALID_ARG;
+  if (d->mode < FAK_DECODE_ONE_LAUNCH || d->mode > FAK_DECODE_PER_MATMUL_I8X) return FAK_ERR_INVALID_ARG;
   auto okdim = [](int64_t v) { return v >= 256 && v % 256 == 0 && v <= FAK_ENGINE_MAX_K; };
   if (d->n_layers < 0 || !okdim(d->d_model) || !okdim(d->d_ff) || !okdim(d->n_mix) || d->vocab < 1 ||
       d->gdn_in < 1 || d->fa_qg < 1 || d->fa_kv < 1)
@@ -1228,13 +1365,14 @@ extern "C" int fak_decode_create(const fak_decode_desc* d, fak_decode** out) {
   c->layers.assign(d->layers, d->layers + d->n_layers);
   c->desc.layers = c->layers.data();
   c->sms = sms;
-  c->mode = d->mode;
+  c->mode = d->mode & 1;  // the _I8X modes are the two launch shapes with int8 activations
+  c->i8x = d->mode >= FAK_DECODE_ONE_LAUNCH_I8X;
   c->n_fa = n_fa;
-  if (d->mode == FAK_DECODE_ONE_LAUNCH) {
+  if (c->mode == FAK_DECODE_ONE_LAUNCH) {
     int dev = 0, coop = 0, per_sm = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, engine_kernel, kThreads, kSmemAlloc);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, engine_kernel<false>, kThreads, kSmemAlloc);
     if (!coop || per_sm < 1) {
       delete c;
       return FAK_ERR_UNSUPPORTED;
@@ -1334,13 +1472,13 @@ extern "C" int fak_decode_step(fak_decode* c, const int32_t* tok_in, int32_t* to
     P.sync = c->sync;
     P.n_ops = c->n_ops;
     P.first_wait = 0;
-    return launch_engine(P, c->sms, true, s);
+    return launch_engine(P, c->sms, true, s, c->i8x);
   }
   for (int i = 0; i < c->n_ops; ++i) {
     P.ops = c->d_ops + i;
     P.n_ops = 1;
     P.sync = nullptr;
-    int st = launch_engine(P, c->sms, false, s);
+    int st = launch_engine(P, c->sms, false, s, c->i8x);
     if (st != FAK_OK) return st;
   }
   return FAK_OK;
