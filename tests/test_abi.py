@@ -41,6 +41,9 @@ def test_validation_happens_before_any_device_call(fak):
     assert lib.fak_q4k_gemv(ok_ptr + 4, 16, 256, ok_ptr, ok_ptr, None) == 3
     assert lib.fak_q4k_gemv(ok_ptr, 16, 256, ok_ptr + 8, ok_ptr, None) == 3
     assert lib.fak_q8_0_gemv(ok_ptr, 16, 288, ok_ptr, ok_ptr, None) == 2
+    assert lib.fak_q4k_gemv_i8x(ok_ptr, 16, 300, ok_ptr, ok_ptr, None) == 2
+    assert lib.fak_q4k_gemv_i8x(ok_ptr + 4, 16, 256, ok_ptr, ok_ptr, None) == 3
+    assert lib.fak_q4k_gemv_i8x(None, 16, 256, ok_ptr, ok_ptr, None) == 1
     assert lib.fak_q4k_gemv_batch(ok_ptr, 16, 256, ok_ptr, 65, ok_ptr, None) == 2
     assert lib.fak_q4k_gemv_batch(ok_ptr, 16, 256, ok_ptr, 0, ok_ptr, None) == 2
     assert lib.fak_q4k_gemv_batch(ok_ptr, 16, 256, None, 4, ok_ptr, None) == 1
