@@ -947,33 +947,29 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
         ahead_due = false;
       }
       if (pl.split) {
-        // sum each group's segments in slab order: the ends of warp runs inside the group, then the group end
+        // sum each row's segments in slab order (the ends of warp runs inside its group, then the
+        // group end), one thread per (group, output row slot), and write the row
         named_bar_sync(1, kConsumerThreads);
-        for (int gi = ctid; gi < pl.ngroups; gi += kConsumerThreads) {
+        for (int t = ctid; t < pl.ngroups * kSlots; t += kConsumerThreads) {
+          const int gi = t / kSlots, r = t % kSlots;
+          const int r0 = pl.r_lo + gi * g.U;
+          if (r >= nout || r >= min(g.U, pl.r_hi - r0)) continue;
+          const int ru = (r + kSlots / 2) % kSlots;  // the paired up row's slot (SwiGLU steps)
+          const float res = (E.flags & F_RESID) ? ld_cg_f(out_ptr(E, r0 + r)) : 0.0f;
           const int b0 = gi * g.nslab, e = b0 + g.nslab - 1;
-          float v[kSlots];
-#pragma unroll
-          for (int r = 0; r < kSlots; ++r) v[r] = 0.0f;
+          float v = 0.0f, vu = 0.0f;
           int last = -1;
           for (int w = 0; w < kNumConsumerWarps - 1; ++w) {
             const int bw = (int)((int64_t)pl.total * (w + 1) / kNumConsumerWarps) - 1;
             if (bw >= b0 && bw < e && bw > last) {
-#pragma unroll
-              for (int r = 0; r < kSlots; ++r) v[r] += part[bw * kSlots + r];
+              v += part[bw * kSlots + r];
+              vu += part[bw * kSlots + ru];
               last = bw;
             }
           }
-#pragma unroll
-          for (int r = 0; r < kSlots; ++r) v[r] += part[e * kSlots + r];
-          const int r0 = pl.r_lo + gi * g.U;
-          const int nr = min(g.U, pl.r_hi - r0);
-          float res[kSlots];  // residuals loaded together: one L2 round trip, not four
-#pragma unroll
-          for (int r = 0; r < kSlots; ++r)
-            res[r] = ((E.flags & F_RESID) && r < nr) ? ld_cg_f(out_ptr(E, r0 + r)) : 0.0f;
-#pragma unroll
-          for (int r = 0; r < kSlots; ++r)
-            if (r < nout && r < nr) emit(E, P, r0 + r, v[r], v[(r + kSlots / 2) % kSlots], wbv, wbi, res[r]);
+          v += part[e * kSlots + r];
+          vu += part[e * kSlots + ru];
+          emit(E, P, r0 + r, v, vu, wbv, wbi, res);
         }
       }
       if (op.flags & F_ARGMAX) {
