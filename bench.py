@@ -489,9 +489,9 @@ def bench_components(fak, torch, hbm, bf16, which):
 
 
 # dram bytes (read + write) of one full decode launch: the ncu capture of the same engine kernel on the
-# 4-layer stack (profiles/engine_kernel_decode_27b_step.md: 950.63 MB for 945.22 MB of weights), scaled by
+# 4-layer stack (profiles/engine_kernel_decode_27b_step.md: 951.84 MB for 945.22 MB of weights), scaled by
 # weight bytes to the 15.048 GB step.  Set to None whenever the engine kernel changes until re-captured.
-DECODE_TRAFFIC_BYTES = int(950.627072e6 / 945.22368e6 * (15_048_048_640 + 5120 * 4))
+DECODE_TRAFFIC_BYTES = int(951.840512e6 / 945.22368e6 * (15_048_048_640 + 5120 * 4))
 
 
 def main():
