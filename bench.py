@@ -285,18 +285,20 @@ _SAMPLE = {}
 
 
 def cpu_oracle_sample(min_seconds=0.0):
-    """Oracle throughput on this host: passes over one GDN layer of the 27B stack (in_proj, out_proj, gate,
-    up, down; 215 MB of Q4_K) plus 1/64 of the Q8_0 lm_head rows, dequantize + f64 dot, repeated until
-    min_seconds of work (at least one pass).  Returns (weight bytes per second, seconds, threads,
-    description)."""
+    """Oracle throughput on this host: passes over one GDN layer (in_proj, out_proj, gate, up, down) and one
+    full-attention layer (q+gate, k, v, o, gate, up, down) of the 27B stack (615 MB of Q4_K) plus 1/64 of
+    the Q8_0 lm_head rows, dequantize + f64 dot, repeated until min_seconds of work (at least one pass).
+    Returns (weight bytes per second, seconds, threads, description)."""
     import numpy as np
     import oracle
     import synth
-    seed, l = SEED_DECODE, 0
+    seed = SEED_DECODE
     if not _SAMPLE:  # inputs are built once; only the oracle's arithmetic is timed
         mats = []
-        for slot, n, k in ((0, GI, D), (1, D, NM), (4, F, D), (5, F, D), (6, D, F)):
-            mats.append((oracle.q4k_pack(synth.normal(seed, 1000 * l + slot, (n, k), 0.02)), n, k, "q4"))
+        for l, shapes in ((0, ((0, GI, D), (1, D, NM), (4, F, D), (5, F, D), (6, D, F))),
+                          (3, ((0, QG, D), (2, KV, D), (3, KV, D), (1, D, NM), (4, F, D), (5, F, D), (6, D, F)))):
+            for slot, n, k in shapes:
+                mats.append((oracle.q4k_pack(synth.normal(seed, 1000 * l + slot, (n, k), 0.02)), n, k, "q4"))
         nlm = V // 64
         mats.append((oracle.q8_0_pack(synth.normal(seed, 900000, (nlm, D), 0.02)), nlm, D, "q8"))
         _SAMPLE["mats"], _SAMPLE["x"] = mats, synth.normal(seed, 12345, (F,), 1.0)
@@ -312,30 +314,68 @@ def cpu_oracle_sample(min_seconds=0.0):
         if dt >= min_seconds:
             break
     threads = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
-    desc = "oracle (dequantize to f32, f64 dot), %d pass(es) in %.2f s over one GDN layer's 5 Q4_K matrices + " \
-           "1/64 of the Q8_0 lm_head (%.0f MB each), scaled to the %.3f GB per token by bytes" % (
-               passes, dt, nbytes / 1e6, 15.048048640)
+    desc = "oracle (dequantize to f32, f64 dot), %d pass(es) in %.2f s over one GDN layer's 5 and one " \
+           "full-attention layer's 7 Q4_K matrices + 1/64 of the Q8_0 lm_head (%.0f MB a pass), scaled to the " \
+           "%.3f GB per token by bytes" % (passes, dt, nbytes / 1e6, 15.048048640)
     return passes * nbytes / dt, dt, threads, desc
 
 
+def host_decode_model(n_layers=NL, vocab=V, seed=SEED_DECODE):
+    """The 27B-shape stack on the host for the oracle: the same seeded weights as the device model, packed
+    by the oracle's packer; the embedding table holds only the rows looked up (filled on demand)."""
+    import numpy as np
+    import oracle
+    import synth
+    layers = []
+    for l in range(n_layers):
+        fa = l % 4 == 3
+        L = {"kind": oracle.LAYER_FA if fa else oracle.LAYER_GDN}
+        shapes = {"w_in": (0, QG if fa else GI, D), "w_out": (1, D, NM), "w_gate": (4, F, D), "w_up": (5, F, D),
+                  "w_down": (6, D, F)}
+        if fa:
+            shapes.update({"w_k": (2, KV, D), "w_v": (3, KV, D)})
+        for key, (slot, n, k) in shapes.items():
+            L[key] = oracle.q4k_pack(synth.normal(seed, 1000 * l + slot, (n, k), 0.02))
+        layers.append(L)
+    rows = 8192
+    lm = np.concatenate([oracle.q8_0_pack(synth.normal(seed, 900000, (min(rows, vocab - r0), D), 0.02,
+                                                       start=r0 * D)).reshape(-1) for r0 in range(0, vocab, rows)])
+    emb = np.zeros((vocab, D), np.float32)  # untouched pages cost no memory
+    model = oracle.Model(D, F, vocab, GI, QG, KV, NM, layers, lm, emb)
+
+    def need_row(t):
+        emb[t] = synth.normal(seed, 900001, (D,), 1.0, start=t * D)
+    return model, need_row
+
+
 def run_reference(args, rank, world):
-    """The reference arm: the CPU oracle as it stands, each step one bounded sample of the decode workload."""
+    """The reference arm: the CPU oracle as it stands, each step one whole decode token of the 27B-shape stack
+    (all 64 layers and the lm_head, 15.05 GB of Q4_K / Q8_0 weights), free-running from token 0 as the GPU
+    step is; timed on this host's cores.  The host model is built first, outside the timed steps."""
     if rank != 0:
         return
-    token_bytes = 15_048_048_640 + D * 4
-    vals, secs = [], []
-    per_step = min(1.0, 120.0 / max(1, args.warmup + args.steps))  # the whole run stays within a few minutes
+    model, need_row = host_decode_model(args.layers, args.vocab)
+    full = args.layers == NL and args.vocab == V
+    threads = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
+    tok, secs = 0, []
     for i in range(args.warmup + args.steps):
-        bps, dt, threads, desc = cpu_oracle_sample(per_step)
+        need_row(tok)
+        t0 = time.perf_counter()
+        tok = model.decode_token(tok)[0]
+        dt = time.perf_counter() - t0
         if i >= args.warmup:
-            vals.append(bps / token_bytes)
             secs.append(dt)
-    v = statistics.mean(vals)
+    ms = 1e3 * statistics.mean(secs)
+    v = 1e3 / ms
+    desc = "oracle (dequantize to f32, f64 dot), %d whole %d-layer tokens timed one by one (after %d untimed), " \
+           "%.3f GB of weights each" % (args.steps, args.layers, args.warmup, model.weight_bytes() / 1e9)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": 1e3 / v, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "27B-shape hybrid decode step, batch 1 (sampled, scaled by weight bytes)"},
+        "config": {"workload": "27B-shape hybrid decode step, batch 1, whole tokens" if full else
+                   "REDUCED profiling case of the 27B-shape decode step: %d layers, Q8_0 lm_head 5120->%d "
+                   "(not the headline)" % (args.layers, args.vocab)},
         "cpu_baseline": {"value": v, "unit": "tok/s", "cores": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
 
@@ -489,8 +529,8 @@ def bench_components(fak, torch, hbm, bf16, which):
 
 
 # dram bytes (read + write) of one full decode launch: the ncu capture of the same engine kernel on the
-# 4-layer stack (profiles/engine_kernel_decode_27b_step.md: 951.84 MB for 945.22 MB of weights), scaled by
-# weight bytes to the 15.048 GB step.  Set to None whenever the engine kernel changes until re-captured.
+# 4-layer stack (951.84 MB for 945.22 MB of weights), scaled by weight bytes to the 15.048 GB step.
+# Set to None whenever the engine kernel changes until re-captured.
 DECODE_TRAFFIC_BYTES = int(951.840512e6 / 945.22368e6 * (15_048_048_640 + 5120 * 4))
 
 

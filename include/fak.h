@@ -173,8 +173,10 @@ int fak_mlp_decode(const void* Wgate, const void* Wup, const void* Wdown, int64_
  * It allocates nothing: its scratch is a file-scope device array in the
  * library, sized for d_ff <= FAK_MLP_NOALLOC_MAX_FF (about 74 KB), held on
  * every GPU that loads the library until the process exits.  The first call
- * on a device looks up that array's device address, so make that first call
- * before any stream capture.  Larger d_ff returns FAK_ERR_SHAPE.  All calls
+ * on a device looks up that array's device address and keeps it for the life
+ * of the process, so make that first call before any stream capture; calls
+ * after a cudaDeviceReset() of that device are not supported (the kept
+ * address would be stale).  Larger d_ff returns FAK_ERR_SHAPE.  All calls
  * share the one array: calls that overlap on the GPU (different streams, no
  * ordering between them) race and give wrong results.  Other arguments,
  * limits and results as fak_mlp_decode. */

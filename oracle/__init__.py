@@ -71,6 +71,8 @@ def _load():
         "orc_gemm_q4k_sample": ([P, I64, I64, P, I64, P, I64, P, I64, P, P], None),
         "orc_rmsnorm": ([P, I64, ctypes.c_double, P], None), "orc_swiglu": ([P, P, I64, P], None),
         "orc_argmax_f32": ([P, I64], I64),
+        "orc_quantize_act_i8": ([P, I64, P, P], None),
+        "orc_gemv_q4k_act_i8": ([P, I64, I64, P, P, P], None),
         "orc_decode_token": ([ctypes.POINTER(_Model), I64, P, P, P, P], I64),
         "orc_decode_weight_bytes": ([ctypes.POINTER(_Model)], I64),
     }
@@ -239,6 +241,28 @@ def swiglu(g, u):
 def argmax_f32(v):
     v, pv = _c(v, np.float32)
     return int(_load().orc_argmax_f32(pv, v.size))
+
+
+# ---------------------------------------------------------------- int8 activations
+def quantize_act_i8(x):
+    """(X int8 [n], d f32 [n/32]): per 32-element sub-block d = max|x| / 127 and
+    X = clamp(rint(x * (127 / max|x|)), -127, 127), in f32 (see oracle.h)."""
+    x, px = _c(x, np.float32)
+    assert x.size % 32 == 0
+    X = np.empty(x.size, np.int8)
+    d = np.empty(x.size // 32, np.float32)
+    _load().orc_quantize_act_i8(px, x.size, X.ctypes.data, d.ctypes.data)
+    return X, d
+
+
+def gemv_q4k_act_i8(W, N, K, x):
+    """(y, a) of the GEMV of the int8 activations of x: sum_k What[n,k] * d_j * X_k in f64."""
+    W, pw = _c(W, np.uint8)
+    x, px = _c(x, np.float32)
+    y = np.empty(N, np.float64)
+    a = np.empty(N, np.float64)
+    _load().orc_gemv_q4k_act_i8(pw, N, K, px, y.ctypes.data, a.ctypes.data)
+    return y, a
 
 
 # ---------------------------------------------------------------- decode stack

@@ -322,6 +322,59 @@ int64_t orc_argmax_f32(const float* v, int64_t n) {
     return best;
 }
 
+/* ------------------------------------------------------ int8 activations */
+
+void orc_quantize_act_i8(const float* x, int64_t n, int8_t* X, float* d) {
+    for (int64_t j = 0; j < n / 32; j++) {
+        const float* xs = x + 32 * j;
+        float am = 0.0f;
+        for (int i = 0; i < 32; i++) {
+            float v = fabsf(xs[i]);
+            if (v > am) am = v;
+        }
+        if (!(am > 0.0f)) {
+            d[j] = 0.0f;
+            for (int i = 0; i < 32; i++) X[32 * j + i] = 0;
+            continue;
+        }
+        float inv = 127.0f / am;
+        d[j] = am / 127.0f;
+        for (int i = 0; i < 32; i++) {
+            float s = xs[i] * inv;
+            X[32 * j + i] = (int8_t)imax(-127, imin(127, (int)rintf(s)));
+        }
+    }
+}
+
+void orc_gemv_q4k_act_i8(const uint8_t* W, int64_t N, int64_t K, const float* x, double* y, double* a) {
+    int8_t* X = (int8_t*)malloc((size_t)K);
+    float* d = (float*)malloc(sizeof(float) * (size_t)(K / 32));
+    double* xq = (double*)malloc(sizeof(double) * (size_t)K);
+    orc_quantize_act_i8(x, K, X, d);
+    for (int64_t k = 0; k < K; k++) xq[k] = (double)d[k / 32] * (double)X[k];
+    int64_t nb = K / 256;
+#pragma omp parallel
+    {
+        float* row = (float*)malloc(sizeof(float) * K);
+#pragma omp for schedule(static)
+        for (int64_t n = 0; n < N; n++) {
+            for (int64_t b = 0; b < nb; b++) orc_q4k_dequant_block(W + (n * nb + b) * 144, row + 256 * b);
+            double s = 0.0, sa = 0.0;
+            for (int64_t k = 0; k < K; k++) {
+                double p = (double)row[k] * xq[k];
+                s += p;
+                sa += fabs(p);
+            }
+            y[n] = s;
+            if (a) a[n] = sa;
+        }
+        free(row);
+    }
+    free(X);
+    free(d);
+    free(xq);
+}
+
 /* ------------------------------------------------------------- decode */
 
 static void to_f32(const double* a, int64_t n, float* out) {

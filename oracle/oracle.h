@@ -75,6 +75,17 @@ void orc_swiglu(const double* g, const double* u, int64_t n, double* out);
 /* index of the largest value; the lowest index wins ties; NaNs are skipped. */
 int64_t orc_argmax_f32(const float* v, int64_t n);
 
+/* int8 activations of the int8-SDOT decode GEMV ("Qwen3.6-27B on Apple M3 Pro",
+ * reconciliation table; the pages give no granularity or rounding, so this is
+ * the reading taken): per 32-element sub-block j of x (n % 32 == 0),
+ *   am_j = max |x_i|,  d_j = am_j / 127,  X_i = clamp(rint(x_i * (127 / am_j)), -127, 127)
+ * in f32 (each division and the product one IEEE-rounded operation, rint ties to
+ * even); d_j = 0 and X = 0 for an all-zero sub-block.  X[n], d[n/32]. */
+void orc_quantize_act_i8(const float* x, int64_t n, int8_t* X, float* d);
+/* y[n] = sum_k What[n,k] * (d_j * X_k) in f64 with (X, d) = orc_quantize_act_i8(x):
+ * the GEMV of the int8 activations; a[n] = sum_k |What[n,k] * d_j * X_k|. */
+void orc_gemv_q4k_act_i8(const uint8_t* W, int64_t N, int64_t K, const float* x, double* y, double* a);
+
 /* ---- one decode token of the hybrid stack ---- */
 enum { ORC_LAYER_GDN = 0, ORC_LAYER_FA = 1 };
 typedef struct {

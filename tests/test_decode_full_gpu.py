@@ -82,14 +82,17 @@ def host_stack(fak, n_layers):
 
 def run_against_oracle(fak, n_layers, n_tokens):
     lo, lg, lmo = host_stack(fak, n_layers)
-    # embedding: the device table from the device twin of the generator; the oracle's table holds
-    # only the rows it reads, from the host generator (the rest stays zero and unread)
+    # embedding: both sides read the same bytes for every token they look up.  The rows a step reads
+    # come from the host generator and are written into the oracle's table and into the device table
+    # before that step; the rest of the device table comes from the device twin of the generator and
+    # is never read (the oracle's stays zero).
     emb_g = torch.empty(V * D, dtype=torch.float32, device="cuda")
     synth.normal_device(emb_g, SEED, 900001, 1.0)
     emb_o = np.zeros((V, D), np.float32)
 
     def need_row(t):
         emb_o[t] = synth.normal(SEED, 900001, (D,), 1.0, start=t * D)
+        emb_g[t * D:(t + 1) * D].copy_(torch.from_numpy(emb_o[t]))
 
     om = oracle.Model(D, F, V, GI, QG, KV, NM, lo, lmo, emb_o)
     ctx = fak.DecodeContext(D, F, V, GI, QG, KV, NM, lg, dev(lmo), emb_g, mode=fak.FAK_DECODE_ONE_LAUNCH)

@@ -3,8 +3,9 @@
 becomes d * X with d = max|x| / 127 and X = rint(x * (127 / max|x|)).
 
 1. The GEMV equals the oracle's GEMV of those quantized activations within the f32 bar
-   (1e-5 * sum|w x~| + 1e-6, cosine >= 0.999999): the quantization is written out here
-   in numpy f32 with the same operations, so the integer dot itself is checked exactly.
+   (1e-5 * sum|w x~| + 1e-6, cosine >= 0.999999): the oracle quantizes x itself
+   (oracle.quantize_act_i8, pinned by hand cases and its half-step bound) and dots the
+   dequantized weights with d * X in f64, so the integer dot itself is checked exactly.
 2. Against the unquantized x the variant is held to a cosine bound only, as on the
    pages (N(0,1) activations: cosine >= 0.9999).
 3. The decode step with int8 activations: one launch equals one launch per matmul bit
@@ -35,17 +36,6 @@ def dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-def quantize_x(x):
-    """The activations the int8 path multiplies: per 32 elements d * X, in f32 as the kernel does."""
-    x32 = np.ascontiguousarray(x, np.float32).reshape(-1, 32)
-    am = np.abs(x32).max(axis=1)
-    with np.errstate(divide="ignore"):
-        qs = np.where(am > 0, np.float32(127) / am, np.float32(0)).astype(np.float32)
-    X = np.clip(np.rint((x32 * qs[:, None]).astype(np.float32)), -127, 127)
-    d = (am / np.float32(127)).astype(np.float32)
-    return (d[:, None].astype(np.float64) * X).astype(np.float32).ravel()
-
-
 def cosine(a, b):
     a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
     return float((a * b).sum() / np.sqrt((a * a).sum() * (b * b).sum()))
@@ -64,7 +54,7 @@ def test_gemv_i8x_is_the_gemv_of_quantized_x(fak, N, K):
     W = oracle.q4k_pack(synth.normal(50, N + K, (N, K), 0.02))
     x = synth.normal(51, N + K, (K,), 1.0)
     y = gemv_i8x(fak, W, N, K, x)
-    yq, aq = oracle.gemv_q4k(W, N, K, quantize_x(x))
+    yq, aq = oracle.gemv_q4k_act_i8(W, N, K, x)
     check_f32(y, yq, aq, "i8x gemv %dx%d vs quantized x" % (N, K))
     ye, _ = oracle.gemv_q4k(W, N, K, x)
     assert cosine(y, ye) >= 0.9999, cosine(y, ye)
@@ -79,7 +69,7 @@ def test_gemv_i8x_awkward_activations(fak):
               np.full(K, -2.5), rng.normal(0, 1e-30, K)):
         x = x.astype(np.float32)
         y = gemv_i8x(fak, W, N, K, x)
-        yq, aq = oracle.gemv_q4k(W, N, K, quantize_x(x))
+        yq, aq = oracle.gemv_q4k_act_i8(W, N, K, x)
         check_f32(y, yq, aq, "i8x awkward activations")
 
 

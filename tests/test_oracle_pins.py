@@ -436,3 +436,61 @@ def test_decode_weight_bytes_match_pages_figure():
     assert b == 15_048_048_640
     assert abs(b - 15e9) / 15e9 < 0.05          # "~15 GB of weights per token"
     assert b < 15.4e9                            # the whole q4_k_m file is 15.4 GB
+
+
+# ------------------------------------------------------------------ int8 activations
+def test_act_i8_hand_cases():
+    # sub-block maxima chosen so that 127 / max is a power of two: the products x * (127 / max)
+    # are exact and every rounding below, ties to even included, is decided by hand
+    x = np.zeros(128, np.float32)
+    x[0:9] = [127, 2.5, 3.5, -2.5, -0.5, 0.5, 1.5, -1.5, 126.25]        # max 127: scale 1, d = 1
+    x[32:37] = [254, 5, 7, -3, 1]                                         # max 254: scale 1/2, d = 2
+    x[64:67] = [-63.5, 1.25, 0.75]                                        # max 63.5: scale 2, d = 1/2
+    # x[96:128] all zero: d = 0, X = 0
+    X, d = oracle.quantize_act_i8(x)
+    want = np.zeros(128, np.int8)
+    want[0:9] = [127, 2, 4, -2, 0, 0, 2, -2, 126]
+    want[32:37] = [127, 2, 4, -2, 0]
+    want[64:67] = [-127, 2, 2]
+    assert np.array_equal(X, want)
+    assert d.tolist() == [1.0, 2.0, 0.5, 0.0]
+
+
+def test_act_i8_bound_range_and_symmetry():
+    rng = np.random.default_rng(40)
+    K = 4096
+    cases = [rng.normal(0, 1, K), rng.standard_t(1.5, K), rng.normal(0, 1, K) * np.repeat(
+        10.0 ** rng.integers(-20, 20, K // 32), 32), np.where(rng.uniform(size=K) < 0.9, 0.0, rng.normal(0, 50, K)),
+        np.full(K, -3.0)]
+    for x in cases:
+        x = x.astype(np.float32)
+        X, d = oracle.quantize_act_i8(x)
+        assert X.min() >= -127 and X.max() <= 127
+        dd = np.repeat(d.astype(np.float64), 32)
+        err = np.abs(x.astype(np.float64) - dd * X)
+        # half a step, plus the f32 roundings of 127/max and of the product (a few ulps of max|x|)
+        am = np.repeat(np.abs(x.reshape(-1, 32)).max(axis=1).astype(np.float64), 32)
+        assert np.all(err <= dd / 2 + am * 2.0 ** -21)
+        # the largest element of every non-zero sub-block lands on +-127
+        xs = x.reshape(-1, 32)
+        top = np.abs(xs).argmax(axis=1)
+        nz = np.abs(xs).max(axis=1) > 0
+        assert np.all(np.abs(X.reshape(-1, 32)[np.arange(xs.shape[0]), top][nz]) == 127)
+        Xn, dn = oracle.quantize_act_i8(-x)
+        assert np.array_equal(Xn, -X) and np.array_equal(dn, d)
+
+
+def test_gemv_act_i8_exact_arithmetic():
+    rng = np.random.default_rng(41)
+    N, K = 3, 512
+    W = oracle.q4k_pack(synth.normal(41, 0, (N, K), 0.02))
+    x = rng.standard_t(2.0, K).astype(np.float32)
+    X, d = oracle.quantize_act_i8(x)
+    xq = [Fraction(float(d[k // 32])) * int(X[k]) for k in range(K)]
+    y, a = oracle.gemv_q4k_act_i8(W, N, K, x)
+    for n in range(N):
+        w = _exact_row(W[n], K)
+        exact = sum(wi * xi for wi, xi in zip(w, xq))
+        sabs = sum(abs(wi * xi) for wi, xi in zip(w, xq))
+        assert abs(Fraction(y[n]) - exact) <= sabs * Fraction(1, 2 ** 23)
+        assert abs(a[n] - float(sabs)) <= float(sabs) * 2 ** -20
