@@ -43,6 +43,17 @@ class _Layer(ctypes.Structure):
                 ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p)]
 
 
+class _MixerDims(ctypes.Structure):
+    _fields_ = [("nk", ctypes.c_int64), ("nv", ctypes.c_int64), ("dk", ctypes.c_int64), ("dv", ctypes.c_int64),
+                ("conv", ctypes.c_int64), ("nq", ctypes.c_int64), ("nkv", ctypes.c_int64), ("dh", ctypes.c_int64),
+                ("rot", ctypes.c_int64), ("theta", ctypes.c_double), ("eps", ctypes.c_double)]
+
+
+class _MixerParams(ctypes.Structure):
+    _fields_ = [("conv_w", ctypes.c_void_p), ("a_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+                ("norm_w", ctypes.c_void_p), ("q_norm_w", ctypes.c_void_p), ("k_norm_w", ctypes.c_void_p)]
+
+
 class _Model(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int64), ("d_model", ctypes.c_int64), ("d_ff", ctypes.c_int64),
                 ("vocab", ctypes.c_int64), ("gdn_in", ctypes.c_int64), ("fa_qg", ctypes.c_int64),
@@ -72,6 +83,14 @@ def _load():
         "orc_rmsnorm": ([P, I64, ctypes.c_double, P], None), "orc_swiglu": ([P, P, I64, P], None),
         "orc_argmax_f32": ([P, I64], I64),
         "orc_quantize_act_i8": ([P, I64, P, P], None),
+        "orc_causal_conv_step": ([P, P, P, I64, I64, P], None),
+        "orc_gdn_step": ([ctypes.POINTER(_MixerDims), ctypes.POINTER(_MixerParams), P, P, P, P, P], None),
+        "orc_attn_step": ([ctypes.POINTER(_MixerDims), ctypes.POINTER(_MixerParams), P, P, P, I64, I64, P, P, P],
+                          None),
+        "orc_mixer_state_create": ([ctypes.POINTER(_Model), ctypes.POINTER(_MixerDims), I64], P),
+        "orc_mixer_state_destroy": ([P], None),
+        "orc_decode_token_mixer": ([ctypes.POINTER(_Model), ctypes.POINTER(_MixerDims),
+                                    ctypes.POINTER(_MixerParams), P, I64, P, P, P], I64),
         "orc_gemv_q4k_act_i8": ([P, I64, I64, P, P, P], None),
         "orc_decode_token": ([ctypes.POINTER(_Model), I64, P, P, P, P], I64),
         "orc_decode_weight_bytes": ([ctypes.POINTER(_Model)], I64),
@@ -302,3 +321,107 @@ class Model:
 
     def weight_bytes(self):
         return int(_load().orc_decode_weight_bytes(ctypes.byref(self.c)))
+
+
+# ---------------------------------------------------------------- mixer bodies
+class MixerDims:
+    """Head counts and sizes of the two mixer bodies (defaults: the 27B shape)."""
+
+    def __init__(self, nk=16, nv=48, dk=128, dv=128, conv=4, nq=24, nkv=4, dh=256, rot=64, theta=1e7, eps=1e-6):
+        self.nk, self.nv, self.dk, self.dv, self.conv = nk, nv, dk, dv, conv
+        self.nq, self.nkv, self.dh, self.rot, self.theta, self.eps = nq, nkv, dh, rot, theta, eps
+        self.c = _MixerDims(nk, nv, dk, dv, conv, nq, nkv, dh, rot, float(theta), float(eps))
+
+    @property
+    def conv_dim(self):
+        return 2 * self.nk * self.dk + self.nv * self.dv
+
+    @property
+    def gdn_in(self):
+        return self.conv_dim + self.nv * self.dv + 2 * self.nv
+
+
+class MixerParams:
+    """One layer's mixer parameters (f32 numpy arrays, kept alive here)."""
+
+    def __init__(self, conv_w=None, a_log=None, dt_bias=None, norm_w=None, q_norm_w=None, k_norm_w=None):
+        self.arrays = {}
+        vals = {}
+        for name, arr in (("conv_w", conv_w), ("a_log", a_log), ("dt_bias", dt_bias), ("norm_w", norm_w),
+                          ("q_norm_w", q_norm_w), ("k_norm_w", k_norm_w)):
+            if arr is not None:
+                arr = np.ascontiguousarray(arr, dtype=np.float32)
+                self.arrays[name] = arr
+                vals[name] = arr.ctypes.data
+            else:
+                vals[name] = None
+        self.c = _MixerParams(**vals)
+
+
+def causal_conv_step(w, state, x):
+    """y = one step of the depthwise causal conv (w [n, K] f32, state [n, K-1] f64 updated in place)."""
+    w, pw = _c(w, np.float32)
+    x, px = _c(x, np.float64)
+    assert state.dtype == np.float64 and state.flags.c_contiguous
+    n, K = w.shape
+    y = np.empty(n, np.float64)
+    _load().orc_causal_conv_step(pw, state.ctypes.data, px, n, K, y.ctypes.data)
+    return y
+
+
+def gdn_step(dims, params, t, conv_state, S):
+    """One Gated DeltaNet step on f64 arrays; conv_state [conv_dim, conv-1] and S [nv, dk, dv] are
+    updated in place.  Returns (out [nv*dv], o_raw [nv*dv] before the gated norm)."""
+    t, pt = _c(t, np.float64)
+    assert conv_state.dtype == np.float64 and conv_state.flags.c_contiguous
+    assert S.dtype == np.float64 and S.flags.c_contiguous
+    out = np.empty(dims.nv * dims.dv, np.float64)
+    raw = np.empty(dims.nv * dims.dv, np.float64)
+    _load().orc_gdn_step(ctypes.byref(dims.c), ctypes.byref(params.c), pt, conv_state.ctypes.data, S.ctypes.data,
+                         out.ctypes.data, raw.ctypes.data)
+    return out, raw
+
+
+def attn_step(dims, params, qg, k, v, pos, kc, vc):
+    """One gated attention step at position pos; kc, vc [nkv, max_ctx, dh] f64 updated in place."""
+    qg, pq = _c(qg, np.float64)
+    k, pk = _c(k, np.float64)
+    v, pv = _c(v, np.float64)
+    assert kc.dtype == np.float64 and kc.flags.c_contiguous and vc.shape == kc.shape
+    out = np.empty(dims.nq * dims.dh, np.float64)
+    _load().orc_attn_step(ctypes.byref(dims.c), ctypes.byref(params.c), pq, pk, pv, int(pos), kc.shape[1],
+                          kc.ctypes.data, vc.ctypes.data, out.ctypes.data)
+    return out
+
+
+class MixerDecoder:
+    """A decode that runs the mixer bodies: a Model, its MixerDims, one MixerParams per layer, and the
+    recurrent state (conv states, S, KV caches, position) owned by the oracle."""
+
+    def __init__(self, model, dims, params, max_ctx=256):
+        self.model, self.dims, self.params = model, dims, params
+        self._mp = (_MixerParams * len(params))()
+        for i, p in enumerate(params):
+            self._mp[i] = p.c
+        self._st = _load().orc_mixer_state_create(ctypes.byref(model.c), ctypes.byref(dims.c), int(max_ctx))
+
+    def decode_token(self, tok):
+        """(next token, logits f32, logit_abs f64, final hidden f64); the state advances one token."""
+        m = self.model
+        h = np.empty(m.d_model, np.float64)
+        logits = np.empty(m.vocab, np.float32)
+        la = np.empty(m.vocab, np.float64)
+        nxt = _load().orc_decode_token_mixer(ctypes.byref(m.c), ctypes.byref(self.dims.c), self._mp, self._st,
+                                             int(tok), h.ctypes.data, logits.ctypes.data, la.ctypes.data)
+        return int(nxt), logits, la, h
+
+    def close(self):
+        if self._st:
+            _load().orc_mixer_state_destroy(self._st)
+            self._st = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -449,3 +449,243 @@ int64_t orc_decode_weight_bytes(const orc_model* m) {
     }
     return q4 / 256 * 144 + m->vocab * D / 32 * 34;
 }
+
+/* ------------------------------------------------------- mixer bodies */
+
+static double silu(double x) { return x / (1.0 + exp(-x)); }
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+static double softplus(double x) { return x > 20.0 ? x : log1p(exp(x)); }
+
+void orc_causal_conv_step(const float* w, double* state, const double* x, int64_t n, int64_t K, double* y) {
+    for (int64_t c = 0; c < n; c++) {
+        double* s = state + c * (K - 1);
+        const float* wc = w + c * K;
+        double acc = 0.0;
+        for (int64_t j = 0; j < K - 1; j++) acc += (double)wc[j] * s[j];
+        acc += (double)wc[K - 1] * x[c];
+        y[c] = acc;
+        for (int64_t j = 0; j + 1 < K - 1; j++) s[j] = s[j + 1];
+        s[K - 2] = x[c];
+    }
+}
+
+void orc_gdn_step(const orc_mixer_dims* d, const orc_mixer_params* p, const double* t, double* conv_state,
+                  double* S, double* out, double* o_raw) {
+    const int64_t nk = d->nk, nv = d->nv, dk = d->dk, dv = d->dv, K = d->conv;
+    const int64_t conv_dim = 2 * nk * dk + nv * dv;
+    double* y = (double*)malloc(sizeof(double) * conv_dim);
+    /* short causal conv over q|k|v, then silu */
+    orc_causal_conv_step(p->conv_w, conv_state, t, conv_dim, K, y);
+    for (int64_t c = 0; c < conv_dim; c++) y[c] = silu(y[c]);
+    double* q = y;
+    double* k = y + nk * dk;
+    const double* v = y + 2 * nk * dk;
+    const double* z = t + conv_dim;
+    const double* b = z + nv * dv;
+    const double* a = b + nv;
+    /* per key head: L2 normalization; queries also scaled by 1/sqrt(dk) */
+    for (int64_t h = 0; h < nk; h++) {
+        double sq = 0.0, sk = 0.0;
+        for (int64_t i = 0; i < dk; i++) {
+            sq += q[h * dk + i] * q[h * dk + i];
+            sk += k[h * dk + i] * k[h * dk + i];
+        }
+        double rq = 1.0 / sqrt(sq + d->eps) / sqrt((double)dk), rk = 1.0 / sqrt(sk + d->eps);
+        for (int64_t i = 0; i < dk; i++) {
+            q[h * dk + i] *= rq;
+            k[h * dk + i] *= rk;
+        }
+    }
+    double* o = (double*)malloc(sizeof(double) * dv);
+    double* delta = (double*)malloc(sizeof(double) * dv);
+    for (int64_t h = 0; h < nv; h++) {
+        const int64_t kh = h / (nv / nk);
+        const double* qh = q + kh * dk;
+        const double* khv = k + kh * dk;
+        const double* vh = v + h * dv;
+        double* Sh = S + h * dk * dv;                /* Sh[i][j], i over dk, j over dv */
+        const double beta = sigmoid(b[h]);
+        const double g = -exp((double)p->a_log[h]) * softplus(a[h] + (double)p->dt_bias[h]);
+        const double alpha = exp(g);
+        for (int64_t i = 0; i < dk * dv; i++) Sh[i] *= alpha;
+        for (int64_t j = 0; j < dv; j++) {           /* delta = beta (v - S^T k) */
+            double kv = 0.0;
+            for (int64_t i = 0; i < dk; i++) kv += Sh[i * dv + j] * khv[i];
+            delta[j] = beta * (vh[j] - kv);
+        }
+        for (int64_t i = 0; i < dk; i++)             /* S += k delta^T */
+            for (int64_t j = 0; j < dv; j++) Sh[i * dv + j] += khv[i] * delta[j];
+        for (int64_t j = 0; j < dv; j++) {           /* o = S^T q */
+            double acc = 0.0;
+            for (int64_t i = 0; i < dk; i++) acc += Sh[i * dv + j] * qh[i];
+            o[j] = acc;
+        }
+        if (o_raw) memcpy(o_raw + h * dv, o, sizeof(double) * dv);
+        double ss = 0.0;                             /* gated RMSNorm with the swish gate z */
+        for (int64_t j = 0; j < dv; j++) ss += o[j] * o[j];
+        const double r = 1.0 / sqrt(ss / (double)dv + d->eps);
+        for (int64_t j = 0; j < dv; j++)
+            out[h * dv + j] = o[j] * r * (double)p->norm_w[j] * silu(z[h * dv + j]);
+    }
+    free(o);
+    free(delta);
+    free(y);
+}
+
+static void head_rmsnorm(const double* x, int64_t n, double eps, const float* gain, double* out) {
+    double ss = 0.0;
+    for (int64_t i = 0; i < n; i++) ss += x[i] * x[i];
+    const double r = 1.0 / sqrt(ss / (double)n + eps);
+    for (int64_t i = 0; i < n; i++) out[i] = x[i] * r * (double)gain[i];
+}
+
+static void rope(double* x, int64_t rot, int64_t pos, double theta) {
+    const int64_t half = rot / 2;
+    for (int64_t i = 0; i < half; i++) {
+        const double ang = (double)pos * pow(theta, -2.0 * (double)i / (double)rot);
+        const double c = cos(ang), s = sin(ang);
+        const double x1 = x[i], x2 = x[i + half];
+        x[i] = x1 * c - x2 * s;
+        x[i + half] = x2 * c + x1 * s;
+    }
+}
+
+void orc_attn_step(const orc_mixer_dims* d, const orc_mixer_params* p, const double* qg, const double* k,
+                   const double* v, int64_t pos, int64_t max_ctx, double* kc, double* vc, double* out) {
+    const int64_t nq = d->nq, nkv = d->nkv, dh = d->dh;
+    for (int64_t g = 0; g < nkv; g++) {              /* this position's keys and values into the cache */
+        double* kp = kc + (g * max_ctx + pos) * dh;
+        head_rmsnorm(k + g * dh, dh, d->eps, p->k_norm_w, kp);
+        rope(kp, d->rot, pos, d->theta);
+        memcpy(vc + (g * max_ctx + pos) * dh, v + g * dh, sizeof(double) * dh);
+    }
+    double* q = (double*)malloc(sizeof(double) * dh);
+    double* w = (double*)malloc(sizeof(double) * (pos + 1));
+    for (int64_t h = 0; h < nq; h++) {
+        const int64_t g = h / (nq / nkv);
+        head_rmsnorm(qg + h * 2 * dh, dh, d->eps, p->q_norm_w, q);
+        rope(q, d->rot, pos, d->theta);
+        double mx = -INFINITY;
+        for (int64_t s = 0; s <= pos; s++) {
+            const double* kp = kc + (g * max_ctx + s) * dh;
+            double acc = 0.0;
+            for (int64_t i = 0; i < dh; i++) acc += q[i] * kp[i];
+            w[s] = acc / sqrt((double)dh);
+            if (w[s] > mx) mx = w[s];
+        }
+        double sum = 0.0;
+        for (int64_t s = 0; s <= pos; s++) {
+            w[s] = exp(w[s] - mx);
+            sum += w[s];
+        }
+        const double* gate = qg + h * 2 * dh + dh;
+        for (int64_t i = 0; i < dh; i++) {
+            double acc = 0.0;
+            for (int64_t s = 0; s <= pos; s++) acc += w[s] * vc[(g * max_ctx + s) * dh + i];
+            out[h * dh + i] = acc / sum * sigmoid(gate[i]);
+        }
+    }
+    free(q);
+    free(w);
+}
+
+struct orc_mixer_state {
+    int64_t n_layers, max_ctx, pos;
+    double** conv;   /* per layer (GDN) or NULL */
+    double** S;
+    double** kc;     /* per layer (FA) or NULL */
+    double** vc;
+};
+
+orc_mixer_state* orc_mixer_state_create(const orc_model* m, const orc_mixer_dims* d, int64_t max_ctx) {
+    orc_mixer_state* st = (orc_mixer_state*)calloc(1, sizeof(orc_mixer_state));
+    const int64_t L = m->n_layers, conv_dim = 2 * d->nk * d->dk + d->nv * d->dv;
+    st->n_layers = L;
+    st->max_ctx = max_ctx;
+    st->conv = (double**)calloc(L, sizeof(double*));
+    st->S = (double**)calloc(L, sizeof(double*));
+    st->kc = (double**)calloc(L, sizeof(double*));
+    st->vc = (double**)calloc(L, sizeof(double*));
+    for (int64_t l = 0; l < L; l++) {
+        if (m->layers[l].kind == ORC_LAYER_GDN) {
+            st->conv[l] = (double*)calloc(conv_dim * (d->conv - 1), sizeof(double));
+            st->S[l] = (double*)calloc(d->nv * d->dk * d->dv, sizeof(double));
+        } else {
+            st->kc[l] = (double*)calloc(d->nkv * max_ctx * d->dh, sizeof(double));
+            st->vc[l] = (double*)calloc(d->nkv * max_ctx * d->dh, sizeof(double));
+        }
+    }
+    return st;
+}
+
+void orc_mixer_state_destroy(orc_mixer_state* st) {
+    if (!st) return;
+    for (int64_t l = 0; l < st->n_layers; l++) {
+        free(st->conv[l]);
+        free(st->S[l]);
+        free(st->kc[l]);
+        free(st->vc[l]);
+    }
+    free(st->conv);
+    free(st->S);
+    free(st->kc);
+    free(st->vc);
+    free(st);
+}
+
+int64_t orc_decode_token_mixer(const orc_model* m, const orc_mixer_dims* d, const orc_mixer_params* mp,
+                               orc_mixer_state* st, int64_t tok, double* h_out, float* logits,
+                               double* logit_abs) {
+    const int64_t D = m->d_model, F = m->d_ff;
+    int64_t tmax = m->gdn_in > m->fa_qg ? m->gdn_in : m->fa_qg;
+    if (F > tmax) tmax = F;
+    if (m->vocab > tmax) tmax = m->vocab;
+    double* h = (double*)malloc(sizeof(double) * D);
+    double* n = (double*)malloc(sizeof(double) * D);
+    double* o = (double*)malloc(sizeof(double) * D);
+    double* t = (double*)malloc(sizeof(double) * tmax);
+    double* u = (double*)malloc(sizeof(double) * F);
+    double* a = (double*)malloc(sizeof(double) * tmax);
+    double* kk = (double*)malloc(sizeof(double) * m->fa_kv);
+    double* vv = (double*)malloc(sizeof(double) * m->fa_kv);
+    double* mix = (double*)malloc(sizeof(double) * m->n_mix);
+    float* xf = (float*)malloc(sizeof(float) * tmax);
+
+    for (int64_t i = 0; i < D; i++) h[i] = (double)m->embedding[tok * D + i];
+    for (int64_t l = 0; l < m->n_layers; l++) {
+        const orc_layer* L = &m->layers[l];
+        orc_rmsnorm(h, D, m->eps, n);
+        to_f32(n, D, xf);
+        if (L->kind == ORC_LAYER_GDN) {
+            orc_gemv_q4k(L->w_in, m->gdn_in, D, xf, t, NULL);
+            orc_gdn_step(d, &mp[l], t, st->conv[l], st->S[l], mix, NULL);
+        } else {
+            orc_gemv_q4k(L->w_in, m->fa_qg, D, xf, t, NULL);
+            orc_gemv_q4k(L->w_k, m->fa_kv, D, xf, kk, NULL);
+            orc_gemv_q4k(L->w_v, m->fa_kv, D, xf, vv, NULL);
+            orc_attn_step(d, &mp[l], t, kk, vv, st->pos, st->max_ctx, st->kc[l], st->vc[l], mix);
+        }
+        to_f32(mix, m->n_mix, xf);                /* out_proj / o input: the mixer's output */
+        orc_gemv_q4k(L->w_out, D, m->n_mix, xf, o, NULL);
+        for (int64_t i = 0; i < D; i++) h[i] += o[i];
+        orc_rmsnorm(h, D, m->eps, n);
+        to_f32(n, D, xf);
+        orc_gemv_q4k(L->w_gate, F, D, xf, t, NULL);
+        orc_gemv_q4k(L->w_up, F, D, xf, u, NULL);
+        orc_swiglu(t, u, F, a);
+        to_f32(a, F, xf);
+        orc_gemv_q4k(L->w_down, D, F, xf, o, NULL);
+        for (int64_t i = 0; i < D; i++) h[i] += o[i];
+    }
+    st->pos++;
+    if (h_out) memcpy(h_out, h, sizeof(double) * D);
+    orc_rmsnorm(h, D, m->eps, n);
+    to_f32(n, D, xf);
+    orc_gemv_q8_0(m->lm_head, m->vocab, D, xf, t, logit_abs);
+    float* lf = logits ? logits : (float*)malloc(sizeof(float) * m->vocab);
+    to_f32(t, m->vocab, lf);
+    int64_t best = orc_argmax_f32(lf, m->vocab);
+    if (!logits) free(lf);
+    free(h); free(n); free(o); free(t); free(u); free(a); free(kk); free(vv); free(mix); free(xf);
+    return best;
+}

@@ -120,6 +120,77 @@ int64_t orc_decode_token(const orc_model* m, int64_t tok, double* h_out, float* 
 /* Raw bytes of weights one token streams (Q4_K matrices plus the Q8_0 lm_head). */
 int64_t orc_decode_weight_bytes(const orc_model* m);
 
+/* ---- the mixer bodies of the hybrid stack, for the decode that runs them ----
+ * "Qwen3.6-27B on Apple M3 Pro", model architecture list: Gated DeltaNet layers with a
+ * short causal conv (kernel 4), 16 key heads / 48 value heads of 128, an f32 recurrent
+ * state and a swish output gate; full-attention layers with 24 query / 4 KV heads of 256,
+ * an output gate, qk-norm and partial RoPE (a quarter of each head) with theta 1e7.  The
+ * pages name these parts only; the steps below are the published Gated DeltaNet
+ * recurrence (Yang, Kautz and Hatamizadeh, "Gated Delta Networks: Improving Mamba2 with
+ * Delta Rule", ICLR 2025) and gated softmax attention, in the plainest reading (listed
+ * with the other readings in the design notes).  Everything in f64. */
+typedef struct {
+    int64_t nk, nv, dk, dv;   /* GDN key heads, value heads, key dim, value dim */
+    int64_t conv;             /* causal conv taps */
+    int64_t nq, nkv, dh;      /* full-attention query heads, KV heads, head dim */
+    int64_t rot;              /* rotary dims at the front of each attention head */
+    double theta;             /* RoPE base */
+    double eps;               /* epsilon of every norm inside the mixers */
+} orc_mixer_dims;
+typedef struct {              /* per layer; the other kind's fields are NULL */
+    const float* conv_w;      /* GDN [conv_dim][conv], conv_dim = 2*nk*dk + nv*dv */
+    const float* a_log;       /* GDN [nv] */
+    const float* dt_bias;     /* GDN [nv] */
+    const float* norm_w;      /* GDN [dv]: gain of the gated RMSNorm */
+    const float* q_norm_w;    /* FA [dh]: gain of the query RMSNorm */
+    const float* k_norm_w;    /* FA [dh]: gain of the key RMSNorm */
+} orc_mixer_params;
+/* One step of a depthwise causal conv with K taps over n channels: y_c = sum_{j<K-1}
+ * w[c][j]*state[c][j] + w[c][K-1]*x_c (no activation), then state[c] (the last K-1
+ * inputs, oldest first) shifts in x_c.  w [n][K], state [n][K-1]. */
+void orc_causal_conv_step(const float* w, double* state, const double* x, int64_t n, int64_t K, double* y);
+/*
+ * One Gated DeltaNet step.  t = in_proj output, laid out q [nk*dk] | k [nk*dk] |
+ * v [nv*dv] | z [nv*dv] | b [nv] | a [nv].
+ *  conv: channel c of q|k|v: y_c = silu(sum_{j<conv-1} w[c][j]*s[c][j] + w[c][conv-1]*t_c),
+ *        then the state s[c] (the last conv-1 inputs, oldest first) shifts in t_c;
+ *  q, k per key head: x / sqrt(sum x^2 + eps), q further times 1/sqrt(dk);
+ *  per value head h (key head h / (nv/nk)): beta = sigmoid(b_h),
+ *        g = -exp(a_log_h) * softplus(a_h + dt_bias_h),
+ *        S_h = exp(g) S_h;  delta = beta (v_h - S_h^T k);  S_h += k delta^T;  o_h = S_h^T q
+ *        (S_h is dk x dv);
+ *  out_h = o_h / sqrt(mean(o_h^2) + eps) * norm_w * silu(z_h).
+ * conv_state [conv_dim][conv-1] and S [nv][dk][dv] are updated in place; out [nv*dv];
+ * o_raw [nv*dv] (may be NULL) receives o before the gated norm.
+ */
+void orc_gdn_step(const orc_mixer_dims* d, const orc_mixer_params* p, const double* t, double* conv_state,
+                  double* S, double* out, double* o_raw);
+/*
+ * One gated full-attention step at position pos.  qg = q+gate output, per query head h:
+ * q_h = qg[h*2dh, h*2dh+dh), gate_h = qg[h*2dh+dh, (h+1)*2dh); k, v [nkv*dh].
+ *  q_h, k per head: x / sqrt(mean(x^2) + eps) * gain;
+ *  RoPE on dims [0, rot): for i < rot/2, angle = pos * theta^(-2i/rot),
+ *        (x_i, x_{i+rot/2}) -> (x_i cos - x_{i+rot/2} sin, x_{i+rot/2} cos + x_i sin);
+ *  the normed, rotated k and v are written at position pos of kc, vc [nkv][max_ctx][dh];
+ *  query head h reads KV head h / (nq/nkv): scores q.k_p / sqrt(dh) for p <= pos,
+ *        softmax, o_h = sum_p w_p v_p;  out_h = o_h * sigmoid(gate_h).
+ * out [nq*dh].
+ */
+void orc_attn_step(const orc_mixer_dims* d, const orc_mixer_params* p, const double* qg, const double* k,
+                   const double* v, int64_t pos, int64_t max_ctx, double* kc, double* vc, double* out);
+
+/* The recurrent state of a decode that runs the mixer bodies: per GDN layer the conv
+ * state and S, per FA layer the KV cache, and the position.  Zeroed at creation. */
+typedef struct orc_mixer_state orc_mixer_state;
+orc_mixer_state* orc_mixer_state_create(const orc_model* m, const orc_mixer_dims* d, int64_t max_ctx);
+void orc_mixer_state_destroy(orc_mixer_state* st);
+/* orc_decode_token with the mixer bodies: the out_proj / o input is the GDN step's or the
+ * attention step's output instead of t[0:n_mix]; the state advances by one token.
+ * mp: per layer.  Outputs as orc_decode_token. */
+int64_t orc_decode_token_mixer(const orc_model* m, const orc_mixer_dims* d, const orc_mixer_params* mp,
+                               orc_mixer_state* st, int64_t tok, double* h_out, float* logits,
+                               double* logit_abs);
+
 #ifdef __cplusplus
 }
 #endif

@@ -157,17 +157,27 @@ struct Plan {
 __device__ __forceinline__ Plan plan_of(const EngOp& op, const Geo& g, int cw) {
   Plan p;
   const int64_t c = blockIdx.x, G = gridDim.x;
-  const int64_t R0 = op.nrows * c / G, R1 = op.nrows * (c + 1) / G;
+  int64_t R0, R1;
+  if (op.nrows <= 0x7fffffff / (G + 1)) {
+    // every decode step: the products fit 32 bits, and a 32-bit division is a fraction of a 64-bit one
+    const unsigned n = (unsigned)op.nrows, cu = (unsigned)c, Gu = (unsigned)G;
+    R0 = n * cu / Gu;
+    R1 = n * (cu + 1) / Gu;
+  } else {
+    R0 = op.nrows * c / G;
+    R1 = op.nrows * (c + 1) / G;
+  }
   const int64_t ng = (R1 - R0 + g.U - 1) / g.U;
   const int64_t total = ng * g.nslab;
   if (total <= kMaxUnits) {
+    const int t = (int)total;
     p.split = true;
     p.r_lo = (int)R0;
     p.r_hi = (int)R1;
     p.ngroups = (int)ng;
-    p.total = (int)total;
-    p.u0 = (int)(total * cw / kNumConsumerWarps);
-    p.u1 = (int)(total * (cw + 1) / kNumConsumerWarps);
+    p.total = t;
+    p.u0 = t * cw / kNumConsumerWarps;
+    p.u1 = t * (cw + 1) / kNumConsumerWarps;
   } else {
     const int64_t GW = G * kNumConsumerWarps, gw = c * kNumConsumerWarps + cw;
     p.split = false;
@@ -960,7 +970,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           float v = 0.0f, vu = 0.0f;
           int last = -1;
           for (int w = 0; w < kNumConsumerWarps - 1; ++w) {
-            const int bw = (int)((int64_t)pl.total * (w + 1) / kNumConsumerWarps) - 1;
+            const int bw = pl.total * (w + 1) / kNumConsumerWarps - 1;
             if (bw >= b0 && bw < e && bw > last) {
               v += part[bw * kSlots + r];
               vu += part[bw * kSlots + ru];
