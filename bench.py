@@ -39,7 +39,9 @@ if ROOT not in sys.path:
 METRIC = "Q4_K GEMV GB/s (% HBM peak); 27B-shape decode-step tok/s; prefill TFLOPS"
 D, F, V, GI, QG, KV, NM, NL = 5120, 17408, 248320, 16480, 12288, 1024, 6144, 64
 SEED_DECODE = 3
-COMPONENTS = ("gemv", "mlp", "batch", "prefill")
+COMPONENTS = ("gemv", "mlp", "batch", "prefill", "mixer", "prefill_forward")
+# the mixer bodies of the 27B shape: GDN 16 key / 48 value heads of 128, FA 24 query / 4 KV heads of 256
+MIX = dict(gdn_nk=16, gdn_nv=48, fa_nq=24, fa_nkv=4, fa_rot=64, rope_theta=1e7, eps=1e-6)
 
 
 def parse_args():
@@ -270,6 +272,11 @@ def bench_decode(fak, torch, args, dist, rank, world):
     i8_same_tok = int(o1.item()) == int(o2.item())
     ctx_i8.close()
     ctx.close()
+    extra = {}
+    if "mixer" in args.components:
+        extra["decode_with_mixer"] = bench_decode_mixer(fak, torch, args, layers, lm, emb, weight_bytes)
+    if "prefill_forward" in args.components:
+        extra["prefill_forward"] = bench_prefill_forward(fak, torch, args, layers, lm, emb)
     del layers, lm, emb
     torch.cuda.empty_cache()
     algo_bytes = weight_bytes + D * 4  # + the embedding row read per token
@@ -277,7 +284,74 @@ def bench_decode(fak, torch, args, dist, rank, world):
     return {"ms": ms, "tok_s": replica_throughput(world, ms), "clocks": clk.summary(), "algo_bytes": algo_bytes,
             "e2e_tok_s": replica_throughput(world, e2e_ms), "per_matmul_ms": pm_ms,
             "per_matmul_launches": launches_pm, "i8x_ms": i8_ms, "i8x_logits_cosine": i8_cos,
-            "i8x_same_token": i8_same_tok}
+            "i8x_same_token": i8_same_tok, "extra": extra}
+
+
+def mixer_params_device(torch, n_layers, seed=SEED_DECODE):
+    """Seeded mixer parameters per layer on the device (tensor ids 1000*l + 10..15): conv taps 0.5 N(0,1),
+    a_log = log(1 + 15 u), dt_bias N(0,1), gated-norm and qk-norm gains 1 + 0.1 N(0,1)."""
+    import numpy as np
+    import synth
+    conv_dim = 2 * MIX["gdn_nk"] * 128 + MIX["gdn_nv"] * 128
+    out = []
+    for l in range(n_layers):
+        if l % 4 == 3:
+            out.append({"q_norm_w": torch.from_numpy(1.0 + 0.1 * synth.normal(seed, 1000 * l + 14, (256,))).cuda(),
+                        "k_norm_w": torch.from_numpy(1.0 + 0.1 * synth.normal(seed, 1000 * l + 15, (256,))).cuda()})
+        else:
+            u = synth.uniforms(seed, 1000 * l + 11, MIX["gdn_nv"])
+            out.append({"conv_w": torch.from_numpy(0.5 * synth.normal(seed, 1000 * l + 10, (conv_dim, 4))).cuda(),
+                        "a_log": torch.from_numpy(np.log(1.0 + 15.0 * u).astype(np.float32)).cuda(),
+                        "dt_bias": torch.from_numpy(synth.normal(seed, 1000 * l + 12, (MIX["gdn_nv"],))).cuda(),
+                        "norm_w": torch.from_numpy(1.0 + 0.1 * synth.normal(seed, 1000 * l + 13, (128,))).cuda()})
+    return out
+
+
+def bench_decode_mixer(fak, torch, args, layers, lm, emb, weight_bytes):
+    """The same 64-layer step with the mixer bodies running on the GPU inside the launch: the Gated
+    DeltaNet recurrence (conv state + 48 x 128 x 128 f32 state per GDN layer) and gated attention over
+    a GPU-resident KV cache.  Timed over a sequence of `steps` positions from a reset."""
+    mix = dict(MIX, max_ctx=4096, layers=mixer_params_device(torch, args.layers))
+    ctx = fak.DecodeContext(D, F, args.vocab, GI, QG, KV, NM, layers, lm, emb, mode=fak.FAK_DECODE_ONE_LAUNCH,
+                            mixer=mix)
+    tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(args.warmup):
+        ctx.step(tok, tok)
+    ctx.reset()
+    n = max(3, args.steps)
+    ms = time_events(torch, lambda: ctx.step(tok, tok), n, warmup=0)
+    st = ctx.status()
+    if st != 0:
+        raise RuntimeError("mixer decode status %d" % st)
+    ctx.close()
+    n_gdn = sum(1 for l in range(args.layers) if l % 4 != 3)
+    state_bytes = n_gdn * 2 * MIX["gdn_nv"] * 128 * 128 * 4  # S read and written per GDN layer
+    return {"ms_per_step": ms, "tok_s": 1e3 / ms, "positions": n, "weights_bytes": weight_bytes,
+            "gdn_state_bytes": state_bytes,
+            "GBps": (weight_bytes + state_bytes) / (ms * 1e-3) / 1e9}
+
+
+def bench_prefill_forward(fak, torch, args, layers, lm, emb):
+    """The projections-only prefill forward of P tokens through the whole stack as one CUDA graph (the
+    pages' prefill ladder, rung 3: both stage skips set), P = 256 / 512 / 1024."""
+    out = []
+    flops_tok = 0
+    for l in range(args.layers):
+        fa = l % 4 == 3
+        flops_tok += 2 * D * ((QG + 2 * KV) if fa else GI) + 2 * NM * D + 2 * 2 * F * D + 2 * F * D
+    for P in (256, 512, 1024):
+        ctx = fak.PrefillContext(D, F, args.vocab, GI, QG, KV, NM, layers, lm, emb, P)
+        toks = torch.arange(P, dtype=torch.int32, device="cuda") * 7919 % args.vocab
+        tout = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ms = time_events(torch, lambda: ctx.run(toks, tout), 5, warmup=2)
+        st = ctx.status()
+        if st != 0:
+            raise RuntimeError("prefill status %d" % st)
+        out.append({"P": P, "ms": ms, "tok_s": P * 1e3 / ms, "TFLOPs": P * flops_tok / ms / 1e9,
+                    "kernels_per_submission": ctx.kernels(), "submissions": 1})
+        ctx.close()
+        torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
@@ -590,6 +664,8 @@ def main():
         "gpu_launches": args.steps,
         "per_matmul_mode": {"ms_per_step": dec["per_matmul_ms"], "tok_s": 1e3 / dec["per_matmul_ms"],
                             "launches_per_step": dec["per_matmul_launches"]},
+        "decode_with_mixer": dec["extra"].get("decode_with_mixer"),
+        "prefill_forward": dec["extra"].get("prefill_forward"),
         "int8_activation_variant": {"ms_per_step": dec["i8x_ms"], "tok_s": 1e3 / dec["i8x_ms"],
                                     "roofline_frac": dec["algo_bytes"] / (dec["i8x_ms"] * 1e-3) / 1e9 / hbm,
                                     "logits_cosine_vs_exact": dec["i8x_logits_cosine"],

@@ -188,7 +188,8 @@ int fak_mlp_decode_noalloc(const void* Wgate, const void* Wup, const void* Wdown
  * Y = X W^T for P tokens ([diag] section 2: mlp_gate_up_proj and mlp_down_proj
  * dominate prefill; section 4b: the q4k_gemm prefill kernel).
  *   Wq: device Q4_K [N x K]; X: device bf16 [P, K] row-major (bit patterns);
- *   Y: device f32 [P, N].  K % 256 == 0, N % 128 == 0, P >= 1.
+ *   Y: device f32 [P, N].  K % 256 == 0, N >= 1, P >= 1 (a last partial
+ *   128-row tile reads zero-filled rows past N and writes none of them).
  * Tensor cores (tcgen05, bf16 x bf16 -> f32): W is dequantized to bf16 in
  * shared memory, so |error| <= 5e-3 * sum|w_i x_i| + 1e-5.  Deterministic.
  * When there are too few 128 x 256 output tiles to fill the GPU, K is split
@@ -273,7 +274,57 @@ typedef struct {
     const fak_layer_desc* layers; /* host array of n_layers; copied by fak_decode_create */
     const void* lm_head;          /* [vocab x d_model] Q8_0, device */
     const float* embedding;       /* [vocab x d_model] f32, device */
+    const struct fak_mixer_desc* mixer; /* NULL: projections only (the out_proj / o input is
+                                           t[0:n_mix]); else the mixer bodies run, below */
 } fak_decode_desc;
+
+/* ------------------------------------------------------------------ mixer bodies
+ * With desc.mixer set, each layer runs its mixer between the input projections
+ * and out_proj / o ("Qwen3.6-27B on Apple M3 Pro", model architecture list: Gated
+ * DeltaNet layers with a causal conv of 4 taps, key / value heads of 128 and an
+ * f32 recurrent state, a swish output gate; full-attention layers with GQA,
+ * head dim 256, an output gate, qk-norm and partial RoPE; "Mac Qwen3.6-27B Metal
+ * Q4_K perf diagnosis", section 4: the recurrence and attention run on the GPU
+ * inside the one-submission decode).  The steps are the published Gated DeltaNet
+ * recurrence and gated softmax attention; each layer adds one step to the launch.
+ *
+ * GDN layer, in_proj output t laid out q [nk*dk] | k [nk*dk] | v [nv*dv] |
+ * z [nv*dv] | b [nv] | a [nv] (so gdn_in = 2*nk*dk + 2*nv*dv + 2*nv):
+ *   causal conv over q|k|v (taps conv_w[c][0..3], the newest input on tap 3),
+ *   silu; q, k per key head divided by sqrt(sum^2 + eps), q also by sqrt(dk);
+ *   per value head h (key head h / (nv/nk)): beta = sigmoid(b_h),
+ *   g = -exp(a_log_h) * softplus(a_h + dt_bias_h), S_h = exp(g) S_h,
+ *   S_h += k (beta (v_h - S_h^T k))^T, o_h = S_h^T q;
+ *   out_h = o_h / sqrt(mean(o_h^2) + eps) * norm_w * silu(z_h).
+ * FA layer, q+gate output laid out per query head [q (dh) | gate (dh)]:
+ *   q_h and k per head: x / sqrt(mean(x^2) + eps) * gain; RoPE on dims [0, rot)
+ *   (pairs (i, i + rot/2), angle pos * theta^(-2i/rot)); k, v appended to the
+ *   KV cache at the position; query head h attends KV head h / (nq/nkv) over
+ *   positions 0..pos with scores q.k / sqrt(dh); out_h = softmax-weighted v *
+ *   sigmoid(gate_h).
+ * The state (conv states, S, KV cache, position) lives in the context, starts at
+ * zero and advances one token per fak_decode_step; fak_decode_reset clears it.
+ * Supported: dk = dv = 128, dh = 256, conv = 4, nv <= 152 and nq <= 152 (one
+ * CTA per head), nv % nk == 0, nq % nkv == 0, rot even and <= dh,
+ * n_mix == nv*dv == nq*dh.  A step past max_ctx positions records
+ * FAK_ERR_DEVICE (attention uses the first max_ctx positions only).
+ */
+typedef struct {
+    const float* conv_w;     /* GDN: [2*nk*dk + nv*dv][4] f32, device */
+    const float* a_log;      /* GDN: [nv] f32, device */
+    const float* dt_bias;    /* GDN: [nv] f32, device */
+    const float* norm_w;     /* GDN: [dv] f32, device (gated RMSNorm gain) */
+    const float* q_norm_w;   /* FA: [dh] f32, device (query RMSNorm gain) */
+    const float* k_norm_w;   /* FA: [dh] f32, device (key RMSNorm gain) */
+} fak_mixer_layer;
+
+typedef struct fak_mixer_desc {
+    int32_t gdn_nk, gdn_nv, gdn_dk, gdn_dv;  /* GDN key heads, value heads, key dim, value dim */
+    int32_t fa_nq, fa_nkv, fa_dh, fa_rot;    /* FA query heads, KV heads, head dim, rotary dims */
+    float rope_theta, eps;
+    int32_t max_ctx;                         /* KV cache positions */
+    const fak_mixer_layer* layers;           /* host array of n_layers; copied by fak_decode_create */
+} fak_mixer_desc;
 
 typedef struct fak_decode fak_decode;
 
@@ -300,10 +351,17 @@ int fak_decode_step(fak_decode* ctx, const int32_t* d_tok_in, int32_t* d_tok_out
  * so the context stays usable) or FAK_ERR_DEVICE (token id out of range). */
 int fak_decode_status(fak_decode* ctx, fak_stream_t stream);
 
+/* Clears the state a decode with the mixer bodies carries from token to token
+ * (conv states, S, KV cache, position) and the context's tagged buffers, on
+ * `stream`: the next step starts a new sequence at position 0. */
+int fak_decode_reset(fak_decode* ctx, fak_stream_t stream);
+
 /* Copies part of the context's state after a step into dst (host or device
  * memory, caller-owned), stream-ordered on `stream`:
  *   which = 0: the hidden state h [d_model] (before the final norm);
- *   which = 1: the k and v projections of every FA layer, [n_fa][2][fa_kv].
+ *   which = 1: the k and v projections of every FA layer, [n_fa][2][fa_kv];
+ *   which = 2: the mixer output of the last layer, [n_mix] (the out_proj / o
+ *              input; with desc.mixer == NULL, t[0:n_mix] of the last layer).
  * `count` must equal the number of floats of that buffer. */
 int fak_decode_read_state(fak_decode* ctx, int which, float* dst, size_t count, fak_stream_t stream);
 
@@ -321,6 +379,43 @@ int fak_decode_set_timeout_ns(fak_decode* ctx, int64_t ns);
 int fak_decode_debug_unreachable_wait(fak_decode* ctx, int op_index);
 
 void fak_decode_destroy(fak_decode* ctx);
+
+/* ------------------------------------------------------------------ prefill forward
+ * P prompt tokens through the whole stack as ONE submission ("Mac Qwen3.6-27B
+ * Metal Q4_K perf diagnosis", section 4: the resident prefill forward that runs
+ * the whole prefill in one command buffer; "Qwen3.6-27B GDN-hybrid Metal
+ * prefill -- isolation split": the P = 256 / 512 / 1024 ladder, rung 3 with both
+ * stage skips set -- GEMMs and norms only).  Same model description as the
+ * decode (desc.mixer must be NULL: the mixer bodies are left out, the out_proj /
+ * o input is t[:, 0:n_mix]).  Per layer, for every token p:
+ *   n = bf16(rms(h_p)); t = W_in n (FA: also W_k n, W_v n); h_p += W_out bf16(t[0:n_mix]);
+ *   n = bf16(rms(h_p)); h_p += W_down bf16(silu(W_gate n) * (W_up n))
+ * on the tcgen05 dequant-GEMM (bf16 operands, f32 accumulate: the fak_q4k_gemm
+ * error bar per matmul), then logits = lm_head(rms(h_{P-1})) (Q8_0, f32) and the
+ * argmax (lowest index on ties).
+ *
+ * fak_prefill_create allocates the activations for P tokens (1 <= P <= 16384),
+ * an interleaved copy of every layer's gate / up weights (2 * d_ff * d_model /
+ * 256 * 144 bytes per layer, for the SwiGLU fused into the GEMM epilogue), and
+ * records the forward into a CUDA graph.  The weights stay caller-owned and
+ * must outlive the context.  d_model <= 8192.
+ * fak_prefill_run: d_tokens (device int32 [P]) in; d_tok_out (device int32) =
+ * the argmax of the last token's logits; d_logits (device f32 [vocab], nullable).
+ * One graph launch (plus the copies of the tokens in and the results out),
+ * asynchronous on `stream`.
+ * fak_prefill_read_hidden: the final hidden states h [P, d_model] (before the
+ * final norm) into dst (host or device), count = P * d_model.
+ * fak_prefill_kernels: kernel launches in the recorded graph.
+ * fak_prefill_status: synchronizes `stream`, then reads and clears the device
+ * status (FAK_ERR_DEVICE: a token id out of range; FAK_ERR_TIMEOUT: a GEMM wait). */
+typedef struct fak_prefill fak_prefill;
+int fak_prefill_create(const fak_decode_desc* desc, int64_t P, fak_prefill** out);
+int fak_prefill_run(fak_prefill* ctx, const int32_t* d_tokens, int32_t* d_tok_out, float* d_logits,
+                    fak_stream_t stream);
+int fak_prefill_read_hidden(fak_prefill* ctx, float* dst, size_t count, fak_stream_t stream);
+int fak_prefill_kernels(const fak_prefill* ctx);
+int fak_prefill_status(fak_prefill* ctx, fak_stream_t stream);
+void fak_prefill_destroy(fak_prefill* ctx);
 
 /* ------------------------------------------------------------------ status
  * Synchronizes `stream`, then reads and clears the status word shared by the

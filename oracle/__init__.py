@@ -83,6 +83,8 @@ def _load():
         "orc_rmsnorm": ([P, I64, ctypes.c_double, P], None), "orc_swiglu": ([P, P, I64, P], None),
         "orc_argmax_f32": ([P, I64], I64),
         "orc_quantize_act_i8": ([P, I64, P, P], None),
+        "orc_bf16_rne": ([F], U16),
+        "orc_prefill_forward": ([ctypes.POINTER(_Model), P, I64, P, P, P], I64),
         "orc_causal_conv_step": ([P, P, P, I64, I64, P], None),
         "orc_gdn_step": ([ctypes.POINTER(_MixerDims), ctypes.POINTER(_MixerParams), P, P, P, P, P], None),
         "orc_attn_step": ([ctypes.POINTER(_MixerDims), ctypes.POINTER(_MixerParams), P, P, P, I64, I64, P, P, P],
@@ -123,6 +125,10 @@ def f16_rne(v):
 
 def bf16_decode(b):
     return _load().orc_bf16_decode(int(b))
+
+
+def bf16_rne(v):
+    return int(_load().orc_bf16_rne(float(np.float32(v))))
 
 
 # ---------------------------------------------------------------- Q4_K / Q8_0
@@ -321,6 +327,18 @@ class Model:
 
     def weight_bytes(self):
         return int(_load().orc_decode_weight_bytes(ctypes.byref(self.c)))
+
+    def prefill_forward(self, toks):
+        """The projections-only prefill of tokens `toks` (bf16 GEMM operands): (next token, logits of the
+        last token f32, logit_abs f64, final hidden states f64 [P, d_model])."""
+        toks, pt = _c(toks, np.int64)
+        P = toks.size
+        h = np.empty((P, self.d_model), np.float64)
+        logits = np.empty(self.vocab, np.float32)
+        la = np.empty(self.vocab, np.float64)
+        nxt = _load().orc_prefill_forward(ctypes.byref(self.c), pt, P, h.ctypes.data, logits.ctypes.data,
+                                          la.ctypes.data)
+        return int(nxt), logits, la, h
 
 
 # ---------------------------------------------------------------- mixer bodies

@@ -689,3 +689,63 @@ int64_t orc_decode_token_mixer(const orc_model* m, const orc_mixer_dims* d, cons
     free(h); free(n); free(o); free(t); free(u); free(a); free(kk); free(vv); free(mix); free(xf);
     return best;
 }
+
+/* ------------------------------------------------------- prefill forward */
+
+uint16_t orc_bf16_rne(float v) {
+    union { float f; uint32_t u; } c;
+    c.f = v;
+    if ((c.u & 0x7F800000u) == 0x7F800000u && (c.u & 0x7FFFFFu)) return (uint16_t)((c.u >> 16) | 0x40);
+    const uint32_t lsb = (c.u >> 16) & 1u;
+    return (uint16_t)((c.u + 0x7FFFu + lsb) >> 16);
+}
+
+static void rows_to_bf16(const double* a, int64_t rows, int64_t n, int64_t stride, uint16_t* out) {
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t i = 0; i < n; i++) out[r * n + i] = orc_bf16_rne((float)a[r * stride + i]);
+}
+
+int64_t orc_prefill_forward(const orc_model* m, const int64_t* toks, int64_t P, double* h_out, float* logits,
+                            double* logit_abs) {
+    const int64_t D = m->d_model, F = m->d_ff;
+    const int64_t tn = m->gdn_in > m->fa_qg ? m->gdn_in : m->fa_qg;
+    double* h = (double*)malloc(sizeof(double) * P * D);
+    double* n = (double*)malloc(sizeof(double) * P * D);
+    double* t = (double*)malloc(sizeof(double) * P * tn);
+    double* o = (double*)malloc(sizeof(double) * P * D);
+    double* g = (double*)malloc(sizeof(double) * P * F);
+    double* u = (double*)malloc(sizeof(double) * P * F);
+    uint16_t* xb = (uint16_t*)malloc(sizeof(uint16_t) * P * (F > tn ? F : tn));
+    for (int64_t p = 0; p < P; p++)
+        for (int64_t i = 0; i < D; i++) h[p * D + i] = (double)m->embedding[toks[p] * D + i];
+    for (int64_t l = 0; l < m->n_layers; l++) {
+        const orc_layer* L = &m->layers[l];
+        const int64_t nin = L->kind == ORC_LAYER_GDN ? m->gdn_in : m->fa_qg;
+        for (int64_t p = 0; p < P; p++) orc_rmsnorm(h + p * D, D, m->eps, n + p * D);
+        rows_to_bf16(n, P, D, D, xb);
+        orc_gemm_q4k(L->w_in, nin, D, xb, P, t, NULL);
+        rows_to_bf16(t, P, m->n_mix, nin, xb);        /* out_proj / o input: t[:, 0:n_mix] */
+        orc_gemm_q4k(L->w_out, D, m->n_mix, xb, P, o, NULL);
+        for (int64_t i = 0; i < P * D; i++) h[i] += o[i];
+        for (int64_t p = 0; p < P; p++) orc_rmsnorm(h + p * D, D, m->eps, n + p * D);
+        rows_to_bf16(n, P, D, D, xb);
+        orc_gemm_q4k(L->w_gate, F, D, xb, P, g, NULL);
+        orc_gemm_q4k(L->w_up, F, D, xb, P, u, NULL);
+        orc_swiglu(g, u, P * F, g);
+        rows_to_bf16(g, P, F, F, xb);
+        orc_gemm_q4k(L->w_down, D, F, xb, P, o, NULL);
+        for (int64_t i = 0; i < P * D; i++) h[i] += o[i];
+    }
+    if (h_out) memcpy(h_out, h, sizeof(double) * P * D);
+    float* xf = (float*)malloc(sizeof(float) * D);
+    orc_rmsnorm(h + (P - 1) * D, D, m->eps, n);
+    to_f32(n, D, xf);
+    double* y = (double*)malloc(sizeof(double) * m->vocab);
+    orc_gemv_q8_0(m->lm_head, m->vocab, D, xf, y, logit_abs);
+    float* lf = logits ? logits : (float*)malloc(sizeof(float) * m->vocab);
+    to_f32(y, m->vocab, lf);
+    int64_t best = orc_argmax_f32(lf, m->vocab);
+    if (!logits) free(lf);
+    free(h); free(n); free(t); free(o); free(g); free(u); free(xb); free(xf); free(y);
+    return best;
+}

@@ -191,6 +191,22 @@ int64_t orc_decode_token_mixer(const orc_model* m, const orc_mixer_dims* d, cons
                                orc_mixer_state* st, int64_t tok, double* h_out, float* logits,
                                double* logit_abs);
 
+/* ---- the prefill forward, projections only ----
+ * P tokens through the stack in one pass, the mixer bodies left out as in
+ * orc_decode_token (the out_proj / o input is t[0:n_mix]): the matmul-only floor
+ * of the prefill ladder ("Qwen3.6-27B GDN-hybrid Metal prefill -- isolation
+ * split", rung 3: both skips set, GEMMs and norms).  Every matmul input is an
+ * activation rounded to f32 and then to bfloat16 (the prefill GEMM's operand,
+ * orc_gemm_q4k); h stays f64.  Per layer and token p:
+ *   n = bf16(rms(h_p)); t = W_in n; h_p += W_out bf16(t[0:n_mix]);
+ *   n = bf16(rms(h_p)); h_p += W_down bf16(swiglu(W_gate n, W_up n)).
+ * FA layers' k and v projections do not reach any output and are not computed.
+ * Then logits = lm_head(f32(rms(h_{P-1}))) (Q8_0).  h_out [P][d_model] (may be
+ * NULL) receives the final hidden states.  Returns argmax(logits). */
+uint16_t orc_bf16_rne(float v);   /* nearest bfloat16, ties to even (NaN stays NaN) */
+int64_t orc_prefill_forward(const orc_model* m, const int64_t* toks, int64_t P, double* h_out, float* logits,
+                            double* logit_abs);
+
 #ifdef __cplusplus
 }
 #endif

@@ -34,12 +34,23 @@ class LayerDesc(ctypes.Structure):
                 ("w_up", P), ("w_down", P)]
 
 
+class MixerLayer(ctypes.Structure):
+    _fields_ = [("conv_w", P), ("a_log", P), ("dt_bias", P), ("norm_w", P), ("q_norm_w", P), ("k_norm_w", P)]
+
+
+class MixerDesc(ctypes.Structure):
+    _fields_ = [("gdn_nk", ctypes.c_int32), ("gdn_nv", ctypes.c_int32), ("gdn_dk", ctypes.c_int32),
+                ("gdn_dv", ctypes.c_int32), ("fa_nq", ctypes.c_int32), ("fa_nkv", ctypes.c_int32),
+                ("fa_dh", ctypes.c_int32), ("fa_rot", ctypes.c_int32), ("rope_theta", ctypes.c_float),
+                ("eps", ctypes.c_float), ("max_ctx", ctypes.c_int32), ("layers", ctypes.POINTER(MixerLayer))]
+
+
 class DecodeDesc(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("vocab", ctypes.c_int32), ("gdn_in", ctypes.c_int32), ("fa_qg", ctypes.c_int32),
                 ("fa_kv", ctypes.c_int32), ("n_mix", ctypes.c_int32), ("eps", ctypes.c_float),
                 ("mode", ctypes.c_int32), ("layers", ctypes.POINTER(LayerDesc)), ("lm_head", P),
-                ("embedding", P)]
+                ("embedding", P), ("mixer", ctypes.POINTER(MixerDesc))]
 
 
 _SIGS = {
@@ -64,11 +75,18 @@ _SIGS = {
     "fak_decode_step": ([P, P, P, P, P], I32),
     "fak_decode_status": ([P, P], I32),
     "fak_decode_read_state": ([P, I32, P, SZ, P], I32),
+    "fak_decode_reset": ([P, P], I32),
     "fak_decode_launches_per_step": ([P], I32),
     "fak_decode_set_timeout_ns": ([P, I64], I32),
     "fak_decode_debug_unreachable_wait": ([P, I32], I32),
     "fak_decode_destroy": ([P], None),
     "fak_device_status": ([P], I32),
+    "fak_prefill_create": ([ctypes.POINTER(DecodeDesc), I64, ctypes.POINTER(P)], I32),
+    "fak_prefill_run": ([P, P, P, P, P], I32),
+    "fak_prefill_read_hidden": ([P, P, SZ, P], I32),
+    "fak_prefill_kernels": ([P], I32),
+    "fak_prefill_status": ([P, P], I32),
+    "fak_prefill_destroy": ([P], None),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -201,16 +219,30 @@ class DecodeContext:
     w_k, w_v, w_out, w_gate, w_up, w_down (device tensors or pointers)."""
 
     def __init__(self, d_model, d_ff, vocab, gdn_in, fa_qg, fa_kv, n_mix, layers, lm_head, embedding,
-                 eps=1e-6, mode=FAK_DECODE_ONE_LAUNCH):
-        self._keep = (layers, lm_head, embedding)
+                 eps=1e-6, mode=FAK_DECODE_ONE_LAUNCH, mixer=None):
+        """mixer: None (projections only), or a dict with the head counts gdn_nk, gdn_nv, fa_nq, fa_nkv,
+        fa_rot, rope_theta, eps, max_ctx and `layers`: one dict per layer with the device tensors
+        conv_w, a_log, dt_bias, norm_w (GDN layers) or q_norm_w, k_norm_w (FA layers)."""
+        self._keep = (layers, lm_head, embedding, mixer)
         arr = (LayerDesc * max(1, len(layers)))()
         for i, L in enumerate(layers):
             arr[i].kind = L["kind"]
             for key in ("w_in", "w_k", "w_v", "w_out", "w_gate", "w_up", "w_down"):
                 setattr(arr[i], key, _ptr(L.get(key)))
         self._arr = arr
+        mptr = None
+        if mixer is not None:
+            ml = (MixerLayer * max(1, len(layers)))()
+            for i, M in enumerate(mixer["layers"]):
+                for key in ("conv_w", "a_log", "dt_bias", "norm_w", "q_norm_w", "k_norm_w"):
+                    setattr(ml[i], key, _ptr(M.get(key)))
+            self._ml = ml
+            self._md = MixerDesc(mixer["gdn_nk"], mixer["gdn_nv"], 128, 128, mixer["fa_nq"], mixer["fa_nkv"], 256,
+                                 mixer["fa_rot"], float(mixer["rope_theta"]), float(mixer["eps"]), mixer["max_ctx"],
+                                 ctypes.cast(ml, ctypes.POINTER(MixerLayer)))
+            mptr = ctypes.pointer(self._md)
         desc = DecodeDesc(len(layers), d_model, d_ff, vocab, gdn_in, fa_qg, fa_kv, n_mix, float(eps), mode,
-                          ctypes.cast(arr, ctypes.POINTER(LayerDesc)), _ptr(lm_head), _ptr(embedding))
+                          ctypes.cast(arr, ctypes.POINTER(LayerDesc)), _ptr(lm_head), _ptr(embedding), mptr)
         h = P()
         _check(lib.fak_decode_create(ctypes.byref(desc), ctypes.byref(h)), "fak_decode_create")
         self.handle = h
@@ -224,8 +256,13 @@ class DecodeContext:
     def status(self, stream=None):
         return int(lib.fak_decode_status(self.handle, _stream(stream)))
 
+    def reset(self, stream=None):
+        """Start a new sequence: clear the mixer state (conv states, S, KV cache, position)."""
+        _check(lib.fak_decode_reset(self.handle, _stream(stream)), "fak_decode_reset")
+
     def read_state(self, which, dst, stream=None):
-        """which 0: hidden state [d_model]; 1: FA k/v projections [n_fa][2][fa_kv]."""
+        """which 0: hidden state [d_model]; 1: FA k/v projections [n_fa][2][fa_kv]; 2: the last
+        layer's mixer output [n_mix]."""
         count = dst.numel() if hasattr(dst, "numel") else dst.size
         _check(lib.fak_decode_read_state(self.handle, int(which), _ptr(dst), count, _stream(stream)),
                "fak_decode_read_state")
@@ -253,3 +290,50 @@ class DecodeContext:
 
 def fak_decode_create(*args, **kw):
     return DecodeContext(*args, **kw)
+
+
+# ------------------------------------------------------------------ prefill forward
+class PrefillContext:
+    """Owns a fak_prefill context: the projections-only prefill forward of P tokens as one CUDA graph.
+    Same model arguments as DecodeContext (no mixer)."""
+
+    def __init__(self, d_model, d_ff, vocab, gdn_in, fa_qg, fa_kv, n_mix, layers, lm_head, embedding, n_tokens,
+                 eps=1e-6):
+        self._keep = (layers, lm_head, embedding)
+        arr = (LayerDesc * max(1, len(layers)))()
+        for i, L in enumerate(layers):
+            arr[i].kind = L["kind"]
+            for key in ("w_in", "w_k", "w_v", "w_out", "w_gate", "w_up", "w_down"):
+                setattr(arr[i], key, _ptr(L.get(key)))
+        self._arr = arr
+        desc = DecodeDesc(len(layers), d_model, d_ff, vocab, gdn_in, fa_qg, fa_kv, n_mix, float(eps), 0,
+                          ctypes.cast(arr, ctypes.POINTER(LayerDesc)), _ptr(lm_head), _ptr(embedding), None)
+        h = P()
+        _check(lib.fak_prefill_create(ctypes.byref(desc), int(n_tokens), ctypes.byref(h)), "fak_prefill_create")
+        self.handle = h
+        self.P, self.d_model, self.vocab = int(n_tokens), d_model, vocab
+
+    def run(self, tokens, tok_out, logits=None, stream=None):
+        _check(lib.fak_prefill_run(self.handle, _ptr(tokens), _ptr(tok_out), _ptr(logits), _stream(stream)),
+               "fak_prefill_run")
+
+    def read_hidden(self, dst, stream=None):
+        count = dst.numel() if hasattr(dst, "numel") else dst.size
+        _check(lib.fak_prefill_read_hidden(self.handle, _ptr(dst), count, _stream(stream)), "fak_prefill_read_hidden")
+
+    def kernels(self):
+        return int(lib.fak_prefill_kernels(self.handle))
+
+    def status(self, stream=None):
+        return int(lib.fak_prefill_status(self.handle, _stream(stream)))
+
+    def close(self):
+        if self.handle:
+            lib.fak_prefill_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfak.so")
 
-SOURCES = ["engine.cu", "batch.cu", "gemm.cu", "pack.cpp", "pack_device.cu"]
+SOURCES = ["engine.cu", "batch.cu", "gemm.cu", "prefill.cu", "pack.cpp", "pack_device.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -74,12 +74,34 @@ constexpr int kWarmStages = 4;                    // stages per warp warmed in L
 constexpr int kMaxUnits = 200;                    // (row group, slab) units per CTA in split mode
 constexpr int kOffPart = kOffScale + kMaxSuper * 4;
 constexpr int kOffMisc = kOffPart + kMaxUnits * kSlots * 4;
-constexpr int kSmemBytes = kOffMisc + 256;
+constexpr int kOffDesc = kOffMisc + 256;          // the current and the next step's descriptor
+constexpr int kSmemBytes = kOffDesc + 2 * 128;
 constexpr int kSmemAlloc = kSmemBytes + 128;
 static_assert(kSmemAlloc <= 232448, "engine shared memory exceeds the 227 KB per-block limit");
 
-enum OpKind { OP_Q4K = 0, OP_Q4K_SWIGLU = 1, OP_Q8 = 2, OP_EMBED = 3, OP_ARGMAX_REDUCE = 4 };
-enum OpFlag { F_NORM = 1, F_RESID = 2, F_WAIT = 4, F_ARGMAX = 8 };
+enum OpKind { OP_Q4K = 0, OP_Q4K_SWIGLU = 1, OP_Q8 = 2, OP_EMBED = 3, OP_ARGMAX_REDUCE = 4, OP_GDN = 5, OP_ATTN = 6 };
+// F_WAIT: wait for the grid-wide arrival counter before the step; F_NOARRIVE: the CTA does not add
+// to that counter after the step; F_TAGIN / F_TAGOUT: the step's input / outputs carry version tags
+// (below) instead.
+enum OpFlag { F_NORM = 1, F_RESID = 2, F_WAIT = 4, F_ARGMAX = 8, F_TAGIN = 16, F_TAGOUT = 32, F_NOARRIVE = 64 };
+
+// Version tags.  In a multi-step launch a step's outputs are the next step's inputs.  Instead of a
+// grid-wide barrier between the two, every output value carries the parity of its buffer's version
+// in the lowest bit of its f32 significand (a change of at most one unit in the last place), and the
+// consumer polls the values it needs until all of them carry the expected parity.  One bit is
+// enough when every version of a buffer overwrites every element its readers read and each reader
+// reads the same elements at every version: a CTA polling for version v has then already seen
+// version v-1 at each of those elements, and L2 coherence never hands it an older value after a
+// newer one.  (The decode's buffers are laid out so: with the mixer bodies, the full-attention
+// layers' q+gate output has a buffer of its own, because it does not cover the GDN in_proj rows.)
+// Tag of version v of buffer b in token k: (k * writes_per_token(b) + v) & 1, the host passing bit
+// b of (k * writes_per_token(b)) & 1 in EngParams::flip; freshly zeroed buffers hold version 0.
+// tags bits: [2:0] input buffer, [3] input version parity; per output segment s: [4s+6:4s+4] buffer,
+// [4s+7] version parity.
+FAK_DEV uint32_t tag_in_buf(int32_t t) { return (uint32_t)t & 7u; }
+FAK_DEV uint32_t tag_in_par(int32_t t) { return ((uint32_t)t >> 3) & 1u; }
+FAK_DEV uint32_t tag_out_buf(int32_t t, int s) { return ((uint32_t)t >> (4 + 4 * s)) & 7u; }
+FAK_DEV uint32_t tag_out_par(int32_t t, int s) { return ((uint32_t)t >> (7 + 4 * s)) & 1u; }
 
 struct EngOp {
   int32_t kind, flags, K, nseg;
@@ -90,8 +112,11 @@ struct EngOp {
   float* y[3];              // outputs per segment
   const float* x;           // input vector [K] (EMBED: the embedding table)
   float eps;
+  int32_t tags;             // version tags of the input and the output segments (F_TAGIN / F_TAGOUT)
+  int32_t wait_target;      // F_WAIT: arrivals per CTA the step waits for (plus wait_extra)
   int32_t pad;
 };
+static_assert(sizeof(EngOp) == 128, "step descriptors are copied to shared memory as 128 bytes");
 
 struct EngParams {
   const EngOp* ops;         // device array, or NULL to use inl[]
@@ -105,7 +130,29 @@ struct EngParams {
   int* tok_out;
   float* logits;
   unsigned long long timeout_ns;
+  unsigned flip;            // bit b: version-tag flip of buffer b for this token; bit 8: token parity
+  int* pos;                 // decode with the mixer bodies: the token's position (advanced by the argmax step)
   EngOp inl[2];             // used when ops == NULL (at most 2 steps)
+};
+
+// A mixer step's operands (device memory, one per layer; EngOp::x points at it).
+struct MixDesc {
+  const float* t;        // in_proj (GDN) / q+gate (FA) output, tagged
+  const float* kin;      // FA: k projection, tagged
+  const float* vin;      // FA: v projection, tagged
+  float* out;            // the mixer output [n_mix], tagged
+  const float* conv_w;   // GDN: [conv_dim][4]
+  const float* a_log;    // GDN: [nv]
+  const float* dt_bias;  // GDN: [nv]
+  const float* norm_w;   // GDN: [128]
+  float* conv_state;     // GDN: [2][conv_dim][3], double-buffered by token parity
+  float* S;              // GDN: [nv][128][128]
+  const float* q_norm_w; // FA: [256]
+  const float* k_norm_w; // FA: [256]
+  float* kc;             // FA: [nkv][max_ctx][256]
+  float* vc;             // FA: [nkv][max_ctx][256]
+  int32_t nk, nv, nq, nkv, rot, max_ctx;
+  float theta, eps;
 };
 
 __device__ int g_fak_status;  // status word of the stateless entry points
@@ -327,15 +374,19 @@ __device__ __forceinline__ void prefetch_stage_l2(const Cursor& c, int lane) {
 constexpr int kMaxSbPerWarp = (kMaxSuper + kNumConsumerWarps - 1) / kNumConsumerWarps;
 constexpr int kSbBatch = 2;  // super-blocks whose loads are in flight together
 
-// x is read with L1-cached loads: in a multi-step launch they follow the
-// grid-wide acquire, so no line of an earlier step's x can be served stale.
-// One pass over x: every load is issued first, then each super-block is
-// quantized and the warp's share of sum(x^2) is left in red[cw].  The
-// RMSNorm factor is a common scale of the whole vector, so it is applied to
-// the row results in the epilogue instead (the per-super-block power-of-two
-// scales keep the same relative precision either way).
+// An untagged x (the caller's vector, or a step after a grid-wide wait) is read
+// with L1-cached loads: in a multi-step launch they follow the grid-wide
+// acquire, so no line of an earlier step's x can be served stale.  A tagged x
+// (F_TAGIN) is read from L2 and polled until every value carries the expected
+// version tag; a poll that outlasts the timeout records FAK_ERR_TIMEOUT and
+// returns false.  One pass over x: every load is issued first, then each
+// super-block is quantized and the warp's share of sum(x^2) is left in
+// red[cw].  The RMSNorm factor is a common scale of the whole vector, so it is
+// applied to the row results in the epilogue instead (the per-super-block
+// power-of-two scales keep the same relative precision either way).
 template <bool I8>
-__device__ void prepare_x(const EngOp& op, uint8_t* smem, float* red, int cw, int lane) {
+__device__ bool prepare_x(const EngOp& op, const EngParams& P, uint8_t* smem, float* red, int cw, int lane,
+                          volatile int* abort) {
   // int8 activations (the variant of the pages' int8-SDOT decode GEMV) for Q4_K steps only
   const bool i8 = I8 && op.kind != OP_Q8;
   const float* x = op.x;
@@ -344,11 +395,15 @@ __device__ void prepare_x(const EngOp& op, uint8_t* smem, float* red, int cw, in
   float* xS = reinterpret_cast<float*>(smem + kOffS);
   float* xsc = reinterpret_cast<float*>(smem + kOffScale);
   float ss = 0.0f;
+  const bool tagged = op.flags & F_TAGIN;
+  const uint32_t want = tag_in_par(op.tags) ^ ((P.flip >> tag_in_buf(op.tags)) & 1u);
   // the later batches' lines, all requested from L2 now so that their loads hit L1
+  if (!tagged) {
 #pragma unroll
-  for (int k = kSbBatch; k < kMaxSbPerWarp; ++k) {
-    const int sb = cw + k * kNumConsumerWarps;
-    if (sb < nsb) asm volatile("prefetch.global.L1 [%0];" ::"l"(x + sb * 256 + lane * 8));
+    for (int k = kSbBatch; k < kMaxSbPerWarp; ++k) {
+      const int sb = cw + k * kNumConsumerWarps;
+      if (sb < nsb) asm volatile("prefetch.global.L1 [%0];" ::"l"(x + sb * 256 + lane * 8));
+    }
   }
 #pragma unroll 1
   for (int k0 = 0; k0 < kMaxSbPerWarp; k0 += kSbBatch) {
@@ -358,8 +413,46 @@ __device__ void prepare_x(const EngOp& op, uint8_t* smem, float* red, int cw, in
     const int sb = cw + (k0 + k) * kNumConsumerWarps;
     if (sb < nsb) {
       const float* src = x + sb * 256 + lane * 8;
-      va[k] = __ldca(reinterpret_cast<const float4*>(src));
-      vb[k] = __ldca(reinterpret_cast<const float4*>(src + 4));
+      if (tagged) {
+        va[k] = ld_relaxed_f4(src);
+        vb[k] = ld_relaxed_f4(src + 4);
+      } else {
+        va[k] = __ldca(reinterpret_cast<const float4*>(src));
+        vb[k] = __ldca(reinterpret_cast<const float4*>(src + 4));
+      }
+    }
+  }
+  if (tagged) {
+    // poll the super-blocks that still hold an older version until all carry the expected tag
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+      bool all = true;
+#pragma unroll
+      for (int k = 0; k < kSbBatch; ++k) {
+        const int sb = cw + (k0 + k) * kNumConsumerWarps;
+        if (sb < nsb && !__all_sync(0xffffffffu, stale8(va[k], vb[k], want) == 0u)) {
+          all = false;
+          const float* src = x + sb * 256 + lane * 8;
+          va[k] = ld_relaxed_f4(src);
+          vb[k] = ld_relaxed_f4(src + 4);
+        }
+      }
+      if (all) {
+#pragma unroll
+        for (int k = 0; k < kSbBatch; ++k) {
+          va[k] = untag4(va[k]);
+          vb[k] = untag4(vb[k]);
+        }
+        break;
+      }
+      if (*abort) return false;
+      if (it == 0) {
+        t0 = globaltimer_ns();
+      } else if (globaltimer_ns() - t0 > P.timeout_ns) {
+        set_error(P, FAK_ERR_TIMEOUT, abort);
+        return false;
+      }
+      __nanosleep(64);
     }
   }
 #pragma unroll
@@ -453,6 +546,7 @@ __device__ void prepare_x(const EngOp& op, uint8_t* smem, float* red, int cw, in
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if (lane == 0) red[cw] = ss;
+  return true;
 }
 
 // The RMSNorm factor from the warps' partial sums (same order in every thread
@@ -727,10 +821,11 @@ struct EmitInfo {
   int se0, se1;  // segment row ends
   int flags;
   float rn;      // RMSNorm factor (1 without F_NORM)
+  uint32_t tg;   // F_TAGOUT: the version tag of segment s in bit s
   bool pair;
 };
 
-__device__ __forceinline__ EmitInfo emit_info(const EngOp& op, float rn) {
+__device__ __forceinline__ EmitInfo emit_info(const EngOp& op, float rn, unsigned flip) {
   EmitInfo E;
   E.y0 = op.y[0];
   E.y1 = op.y[1];
@@ -739,6 +834,10 @@ __device__ __forceinline__ EmitInfo emit_info(const EngOp& op, float rn) {
   E.se1 = op.nseg > 2 ? (int)op.seg_end[1] : 0x7fffffff;
   E.flags = op.flags;
   E.rn = rn;
+  E.tg = 0;
+#pragma unroll
+  for (int sgi = 0; sgi < 3; ++sgi)
+    E.tg |= (tag_out_par(op.tags, sgi) ^ ((flip >> tag_out_buf(op.tags, sgi)) & 1u)) << sgi;
   E.pair = op.kind == OP_Q4K_SWIGLU;
   return E;
 }
@@ -749,11 +848,22 @@ __device__ __forceinline__ float* out_ptr(const EmitInfo& E, int row) {
   return row < E.se0 ? E.y0 + row : (row < E.se1 ? E.y1 + (row - E.se0) : E.y2 + (row - E.se1));
 }
 
+// The residual of output row `row` (0 without F_RESID): a tagged output is read back untagged.
+__device__ __forceinline__ float resid_load(const EmitInfo& E, int row) {
+  if (!(E.flags & F_RESID)) return 0.0f;
+  const float r = ld_cg_f(out_ptr(E, row));
+  return (E.flags & F_TAGOUT) ? untag(r) : r;
+}
+
 __device__ __forceinline__ void emit(const EmitInfo& E, const EngParams& P, int row, float v, float v_up, float& wbv,
                                      int& wbi, float res) {
   if (E.pair) {
     const float gt = v * E.rn, up = v_up * E.rn;
-    E.y0[row] = gt / (1.0f + expf(-gt)) * up;
+    const float a = gt / (1.0f + expf(-gt)) * up;
+    if (E.flags & F_TAGOUT)
+      st_tagged(E.y0 + row, a, E.tg & 1u);
+    else
+      E.y0[row] = a;
     return;
   }
   float* yp = out_ptr(E, row);
@@ -761,6 +871,9 @@ __device__ __forceinline__ void emit(const EmitInfo& E, const EngParams& P, int 
   if (E.flags & F_ARGMAX) {
     if (P.logits) P.logits[row] = val;
     better(val, row, wbv, wbi);
+  } else if (E.flags & F_TAGOUT) {
+    const int sgi = row < E.se0 ? 0 : (row < E.se1 ? 1 : 2);
+    st_tagged(yp, val, (E.tg >> sgi) & 1u);
   } else {
     *yp = val;
   }
@@ -782,6 +895,247 @@ __device__ __forceinline__ float reduce4(const float (&acc)[kSlots], int lane) {
   keep += __shfl_xor_sync(0xffffffffu, keep, 2);
   keep += __shfl_xor_sync(0xffffffffu, keep, 1);
   return keep;
+}
+
+// ------------------------------------------------------------------ mixer steps
+// One CTA per head; the other CTAs go straight on to the next step (which polls
+// this step's tagged output).  384 threads.  Scratch in the x-record area of
+// shared memory (free between the previous step's last CTA barrier and the next
+// step's x preparation).
+
+// Polls one tagged value until it carries `want`; false on abort or timeout.
+__device__ __forceinline__ bool poll1(const float* p, uint32_t want, float& v, const EngParams& P,
+                                      volatile int* abort) {
+  v = ld_relaxed_f(p);
+  if ((__float_as_uint(v) & 1u) == want) {
+    v = untag(v);
+    return true;
+  }
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(64);
+    v = ld_relaxed_f(p);
+    if ((__float_as_uint(v) & 1u) == want) {
+      v = untag(v);
+      return true;
+    }
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > P.timeout_ns) {
+      set_error(P, FAK_ERR_TIMEOUT, abort);
+      return false;
+    }
+  }
+}
+
+// Sum over the first `nw` warps' values of `v` (block-wide; every thread gets the same sum,
+// summed in warp order).  scratch: at least nw floats; the caller's threads all call it.
+__device__ __forceinline__ float block_sum(float v, int nw, float* scratch, int ctid) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if ((ctid & 31) == 0 && (ctid >> 5) < nw) scratch[ctid >> 5] = v;
+  named_bar_sync(1, kConsumerThreads);
+  float t = 0.0f;
+  for (int w = 0; w < nw; ++w) t += scratch[w];
+  named_bar_sync(1, kConsumerThreads);
+  return t;
+}
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+
+// Gated DeltaNet step of value head h = blockIdx.x: the causal conv of its q, k, v channels,
+// the L2 norms, the gates, the delta-rule update of S_h (dk x dv = 128 x 128, three threads per
+// column, 43 rows each) and the gated RMSNorm of o_h.
+__device__ void gdn_step(const EngParams& P, const EngOp& op, uint8_t* smem, int ctid, volatile int* abort) {
+  const MixDesc& M = *reinterpret_cast<const MixDesc*>(op.x);
+  const int h = blockIdx.x;
+  const int nv = M.nv, nk = M.nk;
+  if (h >= nv) return;
+  const int ratio = nv / nk, kh = h / ratio;
+  const int conv_dim = 2 * nk * 128 + nv * 128;
+  const uint32_t want = tag_in_par(op.tags) ^ ((P.flip >> tag_in_buf(op.tags)) & 1u);
+  const uint32_t otag = tag_out_par(op.tags, 0) ^ ((P.flip >> tag_out_buf(op.tags, 0)) & 1u);
+  const int par = (P.flip >> 8) & 1;
+  float* y = reinterpret_cast<float*>(smem + kOffX);  // [384] conv outputs: q | k | v
+  float* zs = y + 384;                                 // [128] silu(z)
+  float* part = zs + 128;                              // [3][128]
+  float* scr = part + 384;                             // [16] reductions
+  float* gates = scr + 16;                             // [2] beta, alpha
+  // conv channel of this thread: q (key head kh), k (key head kh), v (value head h)
+  const int c = ctid < 128 ? kh * 128 + ctid
+                           : (ctid < 256 ? nk * 128 + kh * 128 + (ctid - 128) : 2 * nk * 128 + h * 128 + (ctid - 256));
+  float xin = 0.0f, zv = 0.0f, bv = 0.0f, av = 0.0f;
+  bool ok = poll1(M.t + c, want, xin, P, abort);
+  if (ok && ctid < 128) ok = poll1(M.t + conv_dim + h * 128 + ctid, want, zv, P, abort);
+  if (ok && ctid == 0) ok = poll1(M.t + conv_dim + nv * 128 + h, want, bv, P, abort);
+  if (ok && ctid == 0) ok = poll1(M.t + conv_dim + nv * 128 + nv + h, want, av, P, abort);
+  named_bar_sync(1, kConsumerThreads);
+  if (*abort) return;
+  {
+    const float* so = M.conv_state + ((size_t)par * conv_dim + c) * 3;
+    float* sn = M.conv_state + ((size_t)(par ^ 1) * conv_dim + c) * 3;
+    const float4 w = *reinterpret_cast<const float4*>(M.conv_w + (size_t)c * 4);
+    const float s0 = so[0], s1 = so[1], s2 = so[2];
+    const float acc = fmaf(w.w, xin, fmaf(w.z, s2, fmaf(w.y, s1, w.x * s0)));
+    y[ctid] = silu_f(acc);
+    // the q and k channels are shared by `ratio` value heads: the first one writes their new state
+    if (ctid >= 256 || h % ratio == 0) {
+      sn[0] = s1;
+      sn[1] = s2;
+      sn[2] = xin;
+    }
+    if (ctid < 128) zs[ctid] = silu_f(zv);
+    if (ctid == 0) {
+      gates[0] = 1.0f / (1.0f + expf(-bv));
+      const float sp = av + M.dt_bias[h];
+      const float soft = sp > 20.0f ? sp : log1pf(expf(sp));
+      gates[1] = expf(-expf(M.a_log[h]) * soft);
+    }
+  }
+  named_bar_sync(1, kConsumerThreads);
+  // L2 norms of q (warps 0-3) and k (warps 4-7)
+  const float yv = y[ctid];
+  float sq = (ctid < 256) ? yv * yv : 0.0f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+  if ((ctid & 31) == 0) scr[ctid >> 5] = sq;
+  named_bar_sync(1, kConsumerThreads);
+  const float qq = (scr[0] + scr[1]) + (scr[2] + scr[3]);
+  const float kk = (scr[4] + scr[5]) + (scr[6] + scr[7]);
+  const float rq = 1.0f / sqrtf(qq + M.eps) / sqrtf(128.0f), rk = 1.0f / sqrtf(kk + M.eps);
+  const float beta = gates[0], alpha = gates[1];
+  // state update: column j, rows [43 r, 43 r + 43)
+  const int j = ctid & 127, r = ctid >> 7;
+  float* Sh = M.S + (size_t)h * 128 * 128;
+  float sreg[43];
+  float kv = 0.0f;
+#pragma unroll
+  for (int ii = 0; ii < 43; ++ii) {
+    const int i = 43 * r + ii;
+    if (i < 128) {
+      sreg[ii] = alpha * Sh[i * 128 + j];
+      kv = fmaf(sreg[ii], y[128 + i] * rk, kv);
+    }
+  }
+  part[r * 128 + j] = kv;
+  named_bar_sync(1, kConsumerThreads);
+  const float kvj = (part[j] + part[128 + j]) + part[256 + j];
+  const float delta = beta * (y[256 + j] - kvj);
+  named_bar_sync(1, kConsumerThreads);  // every thread has read part[] before it is reused
+  float o = 0.0f;
+#pragma unroll
+  for (int ii = 0; ii < 43; ++ii) {
+    const int i = 43 * r + ii;
+    if (i < 128) {
+      const float sv = fmaf(y[128 + i] * rk, delta, sreg[ii]);
+      Sh[i * 128 + j] = sv;
+      o = fmaf(sv, y[i] * rq, o);
+    }
+  }
+  part[r * 128 + j] = o;
+  named_bar_sync(1, kConsumerThreads);
+  const float oj = (part[j] + part[128 + j]) + part[256 + j];
+  // gated RMSNorm over the head (warps 0-3 hold the 128 columns)
+  const float ss = block_sum(ctid < 128 ? oj * oj : 0.0f, 4, scr + 8, ctid);
+  if (ctid < 128) {
+    const float rn = 1.0f / sqrtf(ss / 128.0f + M.eps);
+    st_tagged(M.out + h * 128 + j, oj * rn * M.norm_w[j] * zs[j], otag);
+  }
+}
+
+// Gated attention step of query head h = blockIdx.x at position *P.pos: qk-norm, RoPE, the
+// KV-cache append (by the first query head of each KV group), softmax over positions 0..pos
+// and the sigmoid output gate.
+__device__ void attn_step(const EngParams& P, const EngOp& op, uint8_t* smem, int ctid, volatile int* abort) {
+  const MixDesc& M = *reinterpret_cast<const MixDesc*>(op.x);
+  const int h = blockIdx.x;
+  if (h >= M.nq) return;
+  const int grp = M.nq / M.nkv, g = h / grp;
+  const int pos = *P.pos;
+  if (pos < 0 || pos >= M.max_ctx) {
+    if (ctid == 0) atomicCAS(P.err ? P.err : &g_fak_status, 0, FAK_ERR_DEVICE);
+    return;
+  }
+  const uint32_t want = tag_in_par(op.tags) ^ ((P.flip >> tag_in_buf(op.tags)) & 1u);
+  const uint32_t want_kv = 1u ^ ((P.flip >> 3) & 1u);  // every k / v slice: version 1 of its token
+  const uint32_t otag = tag_out_par(op.tags, 0) ^ ((P.flip >> tag_out_buf(op.tags, 0)) & 1u);
+  float* qs = reinterpret_cast<float*>(smem + kOffX);  // [256] normed, rotated q
+  float* ks = qs + 256;                                // [256] normed, rotated k of this position
+  float* vs = ks + 256;                                // [256]
+  float* gs = vs + 256;                                // [256] sigmoid(gate)
+  float* scr = gs + 256;                               // [32]
+  float* sc = scr + 32;                                // [max_ctx] scores, then weights
+  const int d = ctid;
+  float qv = 0.0f, gv = 0.0f, kv = 0.0f, vv = 0.0f;
+  bool ok = true;
+  if (d < 256) {
+    ok = poll1(M.t + h * 512 + d, want, qv, P, abort);
+    if (ok) ok = poll1(M.t + h * 512 + 256 + d, want, gv, P, abort);
+    if (ok) ok = poll1(M.kin + g * 256 + d, want_kv, kv, P, abort);
+    if (ok) ok = poll1(M.vin + g * 256 + d, want_kv, vv, P, abort);
+  }
+  named_bar_sync(1, kConsumerThreads);
+  if (*abort) return;
+  const float sq = block_sum(d < 256 ? qv * qv : 0.0f, 8, scr, ctid);
+  const float sk = block_sum(d < 256 ? kv * kv : 0.0f, 8, scr + 8, ctid);
+  if (d < 256) {
+    qs[d] = qv / sqrtf(sq / 256.0f + M.eps) * M.q_norm_w[d];
+    ks[d] = kv / sqrtf(sk / 256.0f + M.eps) * M.k_norm_w[d];
+    vs[d] = vv;
+    gs[d] = 1.0f / (1.0f + expf(-gv));
+  }
+  named_bar_sync(1, kConsumerThreads);
+  const int half = M.rot / 2;
+  if (d < half) {
+    // the angle in double precision: pos * theta^(-2d/rot) reaches thousands of radians
+    double sn, cs;
+    sincos((double)pos * pow((double)M.theta, -2.0 * (double)d / (double)M.rot), &sn, &cs);
+    const float c = (float)cs, s = (float)sn;
+    const float q1 = qs[d], q2 = qs[d + half], k1 = ks[d], k2 = ks[d + half];
+    qs[d] = q1 * c - q2 * s;
+    qs[d + half] = q2 * c + q1 * s;
+    ks[d] = k1 * c - k2 * s;
+    ks[d + half] = k2 * c + k1 * s;
+  }
+  named_bar_sync(1, kConsumerThreads);
+  float* kcp = M.kc + (size_t)g * M.max_ctx * 256;
+  float* vcp = M.vc + (size_t)g * M.max_ctx * 256;
+  if (h % grp == 0 && d < 256) {
+    kcp[(size_t)pos * 256 + d] = ks[d];
+    vcp[(size_t)pos * 256 + d] = vs[d];
+  }
+  // scores: warp w takes positions w, w + 12, ...; lane l dims 8l..8l+7
+  const int w = ctid >> 5, lane = ctid & 31;
+  for (int sidx = w; sidx <= pos; sidx += kNumConsumerWarps) {
+    const float* kr = sidx == pos ? ks : kcp + (size_t)sidx * 256;
+    float acc = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc = fmaf(qs[lane * 8 + e], kr[lane * 8 + e], acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) sc[sidx] = acc * 0.0625f;  // 1 / sqrt(256)
+  }
+  named_bar_sync(1, kConsumerThreads);
+  float mx = -INFINITY;
+  for (int sidx = ctid; sidx <= pos; sidx += kConsumerThreads) mx = fmaxf(mx, sc[sidx]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) scr[16 + w] = mx;
+  named_bar_sync(1, kConsumerThreads);
+  mx = scr[16];
+  for (int ww = 1; ww < kNumConsumerWarps; ++ww) mx = fmaxf(mx, scr[16 + ww]);
+  named_bar_sync(1, kConsumerThreads);
+  float se = 0.0f;
+  for (int sidx = ctid; sidx <= pos; sidx += kConsumerThreads) {
+    const float e = expf(sc[sidx] - mx);
+    sc[sidx] = e;
+    se += e;
+  }
+  const float sum = block_sum(se, kNumConsumerWarps, scr, ctid);
+  if (d < 256) {
+    float acc = 0.0f;
+    for (int sidx = 0; sidx <= pos; ++sidx) acc = fmaf(sc[sidx], sidx == pos ? vs[d] : vcp[(size_t)sidx * 256 + d], acc);
+    st_tagged(M.out + h * 256 + d, acc / sum * gs[d], otag);
+  }
 }
 
 // ------------------------------------------------------------------ the steps
@@ -841,15 +1195,26 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
   // its own issue, so "wait_group 2" still means "this unit's stage has landed"
   bool ahead = false;
   bool ahead_due = false;  // warp 0: the early issue waits for the step's release
+  // Step descriptors are read from shared memory: warp 0 copies step 0's now and, during
+  // step i, loads step i+1's (one word per lane), storing it before the step's last CTA
+  // barrier.  Read from global memory after a grid-wide handover, each dependent field
+  // load would be an L2 round trip.
+  uint32_t* sdesc = reinterpret_cast<uint32_t*>(smem + kOffDesc);
+  if (P.ops && cw == 0) sdesc[lane] = __ldcg(reinterpret_cast<const uint32_t*>(P.ops) + lane);
   __syncthreads();
 
   for (int i = 0; i < P.n_ops; ++i) {
-    const EngOp& op = P.ops ? P.ops[i] : P.inl[i];
+    const EngOp& op = P.ops ? *reinterpret_cast<const EngOp*>(smem + kOffDesc + (i & 1) * 128) : P.inl[i];
+    uint32_t next_desc = 0;
+    if (P.ops && cw == 0 && i + 1 < P.n_ops)
+      next_desc = __ldcg(reinterpret_cast<const uint32_t*>(P.ops + i + 1) + lane);
     if (P.ops && lane < 2 && i + 1 + lane < P.n_ops)  // the copy cursor reads them next
       asm volatile("prefetch.global.L1 [%0];" ::"l"(P.ops + i + 1 + lane));
-    // -- wait for the previous step of this launch to finish on every CTA
+    // does thread 0 signal this step's end on the grid-wide counter?
+    const bool arrives = P.sync && !(op.flags & F_NOARRIVE);
+    // -- wait for the earlier steps of this launch to finish on every CTA
     if (ctid == 0 && P.sync && (op.flags & F_WAIT) && (i > 0 || P.first_wait) && !*abort) {
-      const unsigned target = (unsigned)i * G + (unsigned)op.wait_extra;
+      const unsigned target = (unsigned)op.wait_target * G + (unsigned)op.wait_extra;
       if (ld_acquire_gpu(&P.sync[0]) < target) {
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t it = 1; ld_acquire_gpu(&P.sync[0]) < target; ++it) {
@@ -871,7 +1236,12 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       }
       const int64_t D = op.K, c = blockIdx.x;
       const int64_t a = D * c / G, b = D * (c + 1) / G;
-      for (int64_t k = a + ctid; k < b; k += kConsumerThreads) op.y[0][k] = op.x[(int64_t)tok * D + k];
+      if (op.flags & F_TAGOUT) {
+        const uint32_t tg = tag_out_par(op.tags, 0) ^ ((P.flip >> tag_out_buf(op.tags, 0)) & 1u);
+        for (int64_t k = a + ctid; k < b; k += kConsumerThreads) st_tagged(op.y[0] + k, op.x[(int64_t)tok * D + k], tg);
+      } else {
+        for (int64_t k = a + ctid; k < b; k += kConsumerThreads) op.y[0][k] = op.x[(int64_t)tok * D + k];
+      }
     } else if (op.kind == OP_ARGMAX_REDUCE) {
       if (blockIdx.x == 0 && cw == 0) {
         float bv = 0.0f;
@@ -884,14 +1254,25 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           better(ov, oi, bv, bi);
         }
         if (lane == 0 && P.tok_out) *P.tok_out = bi < 0 ? 0 : bi;
+        if (lane == 0 && P.pos) *P.pos += 1;  // the next token's position
       }
-    } else {
-      prepare_x<I8X>(op, smem, red, cw, lane);
+    } else if (op.kind == OP_GDN) {
+      gdn_step(P, op, smem, ctid, abort);
       named_bar_sync(1, kConsumerThreads);
-      const float rn = norm_factor(op, red);
+      if (*abort) break;
+    } else if (op.kind == OP_ATTN) {
+      attn_step(P, op, smem, ctid, abort);
+      named_bar_sync(1, kConsumerThreads);
+      if (*abort) break;
+    } else {
+      // the work split depends on the descriptor only: worked out while x is still arriving
       const Geo g = geo_of(op);
       const Plan pl = plan_of(op, g, cw);
-      const EmitInfo E = emit_info(op, rn);
+      prepare_x<I8X>(op, P, smem, red, cw, lane, abort);
+      named_bar_sync(1, kConsumerThreads);
+      if (*abort) break;
+      const float rn = norm_factor(op, red);
+      const EmitInfo E = emit_info(op, rn, P.flip);
       float* part = reinterpret_cast<float*>(smem + kOffPart);
       const int nout = g.pair ? kSlots / 2 : kSlots;  // output rows per group slot set
       float wbv = 0.0f;
@@ -934,7 +1315,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           } else {
             const float up = __shfl_down_sync(0xffffffffu, v, 16);  // pair: up rows sit 16 lanes higher
             if ((lane & 7) == 0 && rs < nout && rs < nr)
-              emit(E, P, r0 + rs, v, up, wbv, wbi, (E.flags & F_RESID) ? ld_cg_f(out_ptr(E, r0 + rs)) : 0.0f);
+              emit(E, P, r0 + rs, v, up, wbv, wbi, resid_load(E, r0 + rs));
           }
 #pragma unroll
           for (int r = 0; r < kSlots; ++r) acc[r] = 0.0f;
@@ -944,18 +1325,12 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           ++grp;
         }
       }
-      // the warp is done with this step's stages: the buffer of its last one is free,
-      // so the next step's third stage starts loading now, before the grid-wide wait
-      // (warp 0 only after its thread 0 has signalled the step: the release fence
-      // waits for copies its warp has in flight)
+      // the warp is done with this step's stages: the buffer of its last one is free, so
+      // the next step's third stage starts loading at the end of this step, once the
+      // CTA's outputs are written (issuing it, with the copy cursor entering the next
+      // step, would otherwise delay them) and after thread 0's arrival where there is
+      // one (a release fence waits for copies in flight)
       ahead_due = !ahead && ic_ok && pl.u1 > pl.u0;
-      if (ahead_due && cw != 0) {
-        issue_stage(ic, lane, mybuf + ((j + kBuffers - 1) % kBuffers) * kStageBytes);
-        cursor_advance(P, ic, cw, lane);
-        ic_ok = ic.op < P.n_ops;
-        ahead = true;
-        ahead_due = false;
-      }
       if (pl.split) {
         // sum each row's segments in slab order (the ends of warp runs inside its group, then the
         // group end), one thread per (group, output row slot), and write the row
@@ -965,7 +1340,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           const int r0 = pl.r_lo + gi * g.U;
           if (r >= nout || r >= min(g.U, pl.r_hi - r0)) continue;
           const int ru = (r + kSlots / 2) % kSlots;  // the paired up row's slot (SwiGLU steps)
-          const float res = (E.flags & F_RESID) ? ld_cg_f(out_ptr(E, r0 + r)) : 0.0f;
+          const float res = resid_load(E, r0 + r);
           const int b0 = gi * g.nslab, e = b0 + g.nslab - 1;
           float v = 0.0f, vu = 0.0f;
           int last = -1;
@@ -1004,8 +1379,9 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       }
     }
     // -- this CTA finished step i
+    if (P.ops && cw == 0 && i + 1 < P.n_ops) sdesc[((i + 1) & 1) * 32 + lane] = next_desc;
     named_bar_sync(1, kConsumerThreads);
-    if (ctid == 0 && P.sync) red_release_gpu_add(&P.sync[0], 1u);
+    if (ctid == 0 && arrives) red_release_gpu_add(&P.sync[0], 1u);
     if (ahead_due) {
       __syncwarp();
       issue_stage(ic, lane, mybuf + ((j + kBuffers - 1) % kBuffers) * kStageBytes);
@@ -1230,6 +1606,7 @@ extern "C" int fak_mlp_decode(const void* Wgate, const void* Wup, const void* Wd
   P.inl[0].w[1] = static_cast<const uint8_t*>(Wup);
   P.inl[0].eps = eps;
   P.inl[1] = make_matvec(OP_Q4K, Wdown, d_model, d_ff, a, y, F_WAIT);
+  P.inl[1].wait_target = 1;  // the gate / up step's arrival on every CTA
   P.n_ops = 2;
   P.sync = sync;
   cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), (cudaStream_t)stream);
@@ -1288,6 +1665,7 @@ extern "C" int fak_mlp_decode_noalloc(const void* Wgate, const void* Wup, const 
   P.inl[0].w[1] = static_cast<const uint8_t*>(Wup);
   P.inl[0].eps = eps;
   P.inl[1] = make_matvec(OP_Q4K, Wdown, d_model, d_ff, a, y, F_WAIT);
+  P.inl[1].wait_target = 1;  // the gate / up step's arrival on every CTA
   P.n_ops = 2;
   P.sync = sync;
   // the counters must start at zero; the SwiGLU output is fully overwritten
@@ -1317,6 +1695,25 @@ struct fak_decode {
   int* err = nullptr;
   unsigned long long timeout_ns = 1000000000ull;
   int debug_op = -1;
+  // version tags (see the engine kernel): tokens stepped since the buffers were last zeroed, and
+  // the writes per token of each tagged buffer (0 h, 1 t, 2 a, 3 the k / v outputs, 4 mix, 5 t2)
+  uint64_t token = 0;
+  uint32_t writes_per_token[6] = {0, 0, 0, 0, 0, 0};
+  // the mixer bodies (desc.mixer set): their output, the recurrent state and the position
+  bool mixer = false;
+  fak_mixer_desc mdesc;
+  std::vector<fak_mixer_layer> mlayers;
+  float* mix = nullptr;          // [n_mix]
+  // The FA layers' q+gate output, apart from the GDN layers' in_proj output in t: with the mixer
+  // bodies, their readers take parts of it (one head each), and a one-bit version tag is only
+  // sound when every version of a buffer overwrites every element its readers read.
+  float* t2 = nullptr;           // [fa_qg]
+  float* mstate = nullptr;       // per GDN layer: conv state [2][conv_dim][3], then S [nv][128][128]
+  size_t mstate_floats = 0;
+  float* kvcache = nullptr;      // per FA layer: k cache, v cache [nkv][max_ctx][256]
+  size_t kvcache_floats = 0;
+  int* pos = nullptr;
+  MixDesc* d_mix = nullptr;      // per layer
 };
 
 namespace {
@@ -1331,14 +1728,57 @@ void free_ctx(fak_decode* c) {
   cudaFree(c->cand_idx);
   cudaFree(c->sync);
   cudaFree(c->err);
+  cudaFree(c->mix);
+  cudaFree(c->t2);
+  cudaFree(c->mstate);
+  cudaFree(c->kvcache);
+  cudaFree(c->pos);
+  cudaFree(c->d_mix);
   delete c;
 }
 
 int upload_ops(fak_decode* c) {
   std::vector<EngOp> ops = c->h_ops;
   for (auto& o : ops) o.wait_extra = 0;
-  if (c->debug_op >= 0 && c->debug_op < (int)ops.size()) ops[c->debug_op].wait_extra = 1;
+  if (c->debug_op >= 0 && c->debug_op < (int)ops.size()) {
+    EngOp& o = ops[c->debug_op];
+    if (o.flags & F_TAGIN)
+      o.tags ^= 1 << 3;   // wait for a version parity the input never carries
+    else
+      o.wait_extra = 1;   // wait for one more arrival than the grid provides
+  }
   return fak_cuda_status(cudaMemcpy(c->d_ops, ops.data(), sizeof(EngOp) * ops.size(), cudaMemcpyHostToDevice));
+}
+
+// Zeroes the tagged buffers (version 0, tag 0) and restarts the token count.
+int reset_tags(fak_decode* c, cudaStream_t s) {
+  const int64_t D = c->desc.d_model, F = c->desc.d_ff;
+  const int64_t tmax = std::max<int64_t>(c->desc.gdn_in, c->desc.fa_qg);
+  const int64_t nkv = std::max<int64_t>(1, 2LL * c->n_fa * c->desc.fa_kv);
+  cudaError_t e = cudaMemsetAsync(c->h, 0, D * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->t, 0, tmax * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->a, 0, F * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->kv, 0, nkv * 4, s);
+  if (e == cudaSuccess && c->mix) e = cudaMemsetAsync(c->mix, 0, (size_t)c->desc.n_mix * 4, s);
+  if (e == cudaSuccess && c->t2) e = cudaMemsetAsync(c->t2, 0, (size_t)c->desc.fa_qg * 4, s);
+  c->token = 0;
+  return fak_cuda_status(e);
+}
+
+// Zeroes the mixer bodies' state (conv states, S, KV caches) and the position.
+int reset_mixer_state(fak_decode* c, cudaStream_t s) {
+  if (!c->mixer) return FAK_OK;
+  cudaError_t e = cudaSuccess;
+  if (c->mstate_floats) e = cudaMemsetAsync(c->mstate, 0, c->mstate_floats * 4, s);
+  if (e == cudaSuccess && c->kvcache_floats) e = cudaMemsetAsync(c->kvcache, 0, c->kvcache_floats * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->pos, 0, sizeof(int), s);
+  return fak_cuda_status(e);
+}
+
+unsigned tag_flip(const fak_decode* c) {
+  unsigned f = 0;
+  for (int b = 0; b < 6; ++b) f |= (unsigned)((c->token * c->writes_per_token[b]) & 1u) << b;
+  return f | (unsigned)(c->token & 1u) << 8;
 }
 }  // namespace
 
@@ -1366,6 +1806,28 @@ extern "C" int fak_decode_create(const fak_decode_desc* d, fak_decode** out) {
   int sms = 0;
   int st = device_setup(&sms);
   if (st != FAK_OK) return st;
+  if (d->mixer) {
+    const fak_mixer_desc& m = *d->mixer;
+    if (!m.layers) return FAK_ERR_INVALID_ARG;
+    if (m.gdn_dk != 128 || m.gdn_dv != 128 || m.fa_dh != 256 || m.gdn_nk < 1 || m.gdn_nv < 1 ||
+        m.gdn_nv % m.gdn_nk || m.gdn_nv > sms || m.fa_nq < 1 || m.fa_nkv < 1 || m.fa_nq % m.fa_nkv ||
+        m.fa_nq > sms || m.fa_rot < 2 || m.fa_rot % 2 || m.fa_rot > 256 || m.max_ctx < 1 || m.max_ctx > 8192 ||
+        !(m.eps >= 0.0f) || !(m.rope_theta > 0.0f))
+      return FAK_ERR_SHAPE;
+    if ((int64_t)m.gdn_nv * 128 != d->n_mix || (int64_t)m.fa_nq * 256 != d->n_mix ||
+        d->gdn_in != 2 * m.gdn_nk * 128 + 2 * m.gdn_nv * 128 + 2 * m.gdn_nv || d->fa_qg != 2 * m.fa_nq * 256 ||
+        d->fa_kv != m.fa_nkv * 256)
+      return FAK_ERR_SHAPE;
+    for (int l = 0; l < d->n_layers; ++l) {
+      const fak_mixer_layer& M = m.layers[l];
+      if (d->layers[l].kind == FAK_LAYER_GDN) {
+        if (!M.conv_w || !M.a_log || !M.dt_bias || !M.norm_w) return FAK_ERR_INVALID_ARG;
+        if (!aligned16(M.conv_w)) return FAK_ERR_ALIGN;
+      } else if (!M.q_norm_w || !M.k_norm_w) {
+        return FAK_ERR_INVALID_ARG;
+      }
+    }
+  }
   fak_decode* c = new fak_decode();
   c->desc = *d;
   c->layers.assign(d->layers, d->layers + d->n_layers);
@@ -1399,24 +1861,113 @@ extern "C" int fak_decode_create(const fak_decode_desc* d, fak_decode** out) {
   cudaMemset(c->sync, 0, 64);
   cudaMemset(c->err, 0, 64);
   cudaMemset(c->kv, 0, std::max<int64_t>(1, 2LL * n_fa * d->fa_kv) * 4);
+  // the tagged buffers start at version 0 (tag 0): no step can mistake them for its input
+  cudaMemset(c->h, 0, D * 4);
+  cudaMemset(c->t, 0, tmax * 4);
+  cudaMemset(c->a, 0, F * 4);
+  // the mixer bodies: output buffer, recurrent state, KV caches, position, step operands
+  std::vector<MixDesc> mds;
+  if (d->mixer) {
+    c->mixer = true;
+    c->mdesc = *d->mixer;
+    c->mlayers.assign(d->mixer->layers, d->mixer->layers + d->n_layers);
+    c->mdesc.layers = c->mlayers.data();
+    const fak_mixer_desc& m = c->mdesc;
+    const int64_t conv_dim = 2LL * m.gdn_nk * 128 + (int64_t)m.gdn_nv * 128;
+    const size_t gdn_floats = (size_t)(2 * conv_dim * 3 + (int64_t)m.gdn_nv * 128 * 128);
+    const size_t fa_floats = (size_t)2 * m.fa_nkv * m.max_ctx * 256;
+    c->mstate_floats = gdn_floats * (size_t)(d->n_layers - n_fa);
+    c->kvcache_floats = fa_floats * (size_t)n_fa;
+    bool okx = cudaMalloc(&c->mix, (size_t)d->n_mix * 4) == cudaSuccess &&
+               cudaMalloc(&c->t2, (size_t)d->fa_qg * 4) == cudaSuccess &&
+               cudaMalloc(&c->pos, sizeof(int)) == cudaSuccess &&
+               cudaMalloc(&c->d_mix, sizeof(MixDesc) * std::max(1, d->n_layers)) == cudaSuccess &&
+               (!c->mstate_floats || cudaMalloc(&c->mstate, c->mstate_floats * 4) == cudaSuccess) &&
+               (!c->kvcache_floats || cudaMalloc(&c->kvcache, c->kvcache_floats * 4) == cudaSuccess);
+    if (!okx) {
+      (void)cudaGetLastError();
+      free_ctx(c);
+      return FAK_ERR_NOMEM;
+    }
+    cudaMemset(c->mix, 0, (size_t)d->n_mix * 4);
+    cudaMemset(c->t2, 0, (size_t)d->fa_qg * 4);
+    if (reset_mixer_state(c, 0) != FAK_OK || cudaDeviceSynchronize() != cudaSuccess) {
+      free_ctx(c);
+      return FAK_ERR_CUDA;
+    }
+    size_t gi = 0, fi = 0;
+    int fa_l = 0;
+    for (int l = 0; l < d->n_layers; ++l) {
+      MixDesc md;
+      memset(&md, 0, sizeof(md));
+      const fak_mixer_layer& M = m.layers[l];
+      md.t = d->layers[l].kind == FAK_LAYER_GDN ? c->t : c->t2;
+      md.out = c->mix;
+      md.nk = m.gdn_nk;
+      md.nv = m.gdn_nv;
+      md.nq = m.fa_nq;
+      md.nkv = m.fa_nkv;
+      md.rot = m.fa_rot;
+      md.max_ctx = m.max_ctx;
+      md.theta = m.rope_theta;
+      md.eps = m.eps;
+      if (d->layers[l].kind == FAK_LAYER_GDN) {
+        md.conv_w = M.conv_w;
+        md.a_log = M.a_log;
+        md.dt_bias = M.dt_bias;
+        md.norm_w = M.norm_w;
+        md.conv_state = c->mstate + gi;
+        md.S = c->mstate + gi + 2 * conv_dim * 3;
+        gi += gdn_floats;
+      } else {
+        md.kin = c->kv + (2LL * fa_l) * d->fa_kv;
+        md.vin = c->kv + (2LL * fa_l + 1) * d->fa_kv;
+        md.q_norm_w = M.q_norm_w;
+        md.k_norm_w = M.k_norm_w;
+        md.kc = c->kvcache + fi;
+        md.vc = c->kvcache + fi + fa_floats / 2;
+        fi += fa_floats;
+        ++fa_l;
+      }
+      mds.push_back(md);
+    }
+    if (cudaMemcpy(c->d_mix, mds.data(), sizeof(MixDesc) * mds.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
+      free_ctx(c);
+      return FAK_ERR_CUDA;
+    }
+  }
 
-  // the op list: embed, per layer 4 matvec steps, lm_head + argmax, argmax reduce
+  // the op list: embed, per layer 4 matvec steps, lm_head + argmax, argmax reduce.  Each step
+  // hands its output to the next through version tags (no grid-wide wait); only the argmax
+  // reduce waits on the arrival counter, for the lm_head step's per-CTA candidates.
+  enum { B_H = 0, B_T = 1, B_A = 2, B_KV = 3, B_MIX = 4, B_T2 = 5 };
+  uint32_t ver[6] = {0, 0, 0, 0, 0, 0};  // versions written so far in a token
+  auto tag_in = [&](int b) { return (int32_t)(b | (int)(ver[b] & 1u) << 3); };
+  auto tag_out = [&](int sgi, int b) {
+    const uint32_t v = b == B_KV ? 1u : ++ver[b];  // every k / v slice is written once per token
+    return (int32_t)((b | (int)(v & 1u) << 3) << (4 + 4 * sgi));
+  };
+  const int kTagged = F_TAGIN | F_TAGOUT | F_NOARRIVE;
   std::vector<EngOp>& ops = c->h_ops;
   EngOp e;
   memset(&e, 0, sizeof(e));
   e.kind = OP_EMBED;
+  e.flags = F_TAGOUT | F_NOARRIVE;
   e.K = (int)D;
   e.vocab = d->vocab;
   e.x = d->embedding;
   e.y[0] = c->h;
   e.nseg = 1;
+  e.tags = tag_out(0, B_H);
   ops.push_back(e);
   int fa_i = 0;
   for (int l = 0; l < d->n_layers; ++l) {
     const fak_layer_desc& L = c->layers[l];
-    EngOp in = make_matvec(OP_Q4K, L.w_in, L.kind == FAK_LAYER_GDN ? d->gdn_in : d->fa_qg, D, c->h, c->t,
-                           F_NORM | F_WAIT);
+    const bool fa_t2 = c->mixer && L.kind == FAK_LAYER_FA;  // q+gate in its own buffer (see t2)
+    EngOp in = make_matvec(OP_Q4K, L.w_in, L.kind == FAK_LAYER_GDN ? d->gdn_in : d->fa_qg, D, c->h,
+                           fa_t2 ? c->t2 : c->t, F_NORM | kTagged);
     in.eps = d->eps;
+    in.tags = tag_in(B_H) | tag_out(0, fa_t2 ? B_T2 : B_T);
     if (L.kind == FAK_LAYER_FA) {
       in.nseg = 3;
       in.seg_end[0] = d->fa_qg;
@@ -1427,25 +1978,46 @@ extern "C" int fak_decode_create(const fak_decode_desc* d, fak_decode** out) {
       in.w[2] = static_cast<const uint8_t*>(L.w_v);
       in.y[1] = c->kv + (2LL * fa_i) * d->fa_kv;
       in.y[2] = c->kv + (2LL * fa_i + 1) * d->fa_kv;
+      in.tags |= tag_out(1, B_KV) | tag_out(2, B_KV);
       ++fa_i;
     }
     ops.push_back(in);
-    ops.push_back(make_matvec(OP_Q4K, L.w_out, D, d->n_mix, c->t, c->h, F_RESID | F_WAIT));
-    EngOp gu = make_matvec(OP_Q4K_SWIGLU, L.w_gate, F, D, c->h, c->a, F_NORM | F_WAIT);
+    if (c->mixer) {
+      // the mixer body between the projections: reads t (and this layer's k, v), writes mix
+      EngOp mx;
+      memset(&mx, 0, sizeof(mx));
+      mx.kind = L.kind == FAK_LAYER_GDN ? OP_GDN : OP_ATTN;
+      mx.flags = kTagged;
+      mx.nseg = 1;
+      mx.x = reinterpret_cast<const float*>(c->d_mix + l);
+      mx.tags = tag_in(fa_t2 ? B_T2 : B_T) | tag_out(0, B_MIX);
+      ops.push_back(mx);
+    }
+    EngOp out = make_matvec(OP_Q4K, L.w_out, D, d->n_mix, c->mixer ? c->mix : c->t, c->h, F_RESID | kTagged);
+    out.tags = tag_in(c->mixer ? B_MIX : B_T) | tag_out(0, B_H);
+    ops.push_back(out);
+    EngOp gu = make_matvec(OP_Q4K_SWIGLU, L.w_gate, F, D, c->h, c->a, F_NORM | kTagged);
     gu.w[1] = static_cast<const uint8_t*>(L.w_up);
     gu.eps = d->eps;
+    gu.tags = tag_in(B_H) | tag_out(0, B_A);
     ops.push_back(gu);
-    ops.push_back(make_matvec(OP_Q4K, L.w_down, D, F, c->a, c->h, F_RESID | F_WAIT));
+    EngOp dn = make_matvec(OP_Q4K, L.w_down, D, F, c->a, c->h, F_RESID | kTagged);
+    dn.tags = tag_in(B_A) | tag_out(0, B_H);
+    ops.push_back(dn);
   }
-  EngOp lm = make_matvec(OP_Q8, d->lm_head, d->vocab, D, c->h, nullptr, F_NORM | F_WAIT | F_ARGMAX);
+  EngOp lm = make_matvec(OP_Q8, d->lm_head, d->vocab, D, c->h, nullptr, F_NORM | F_TAGIN | F_ARGMAX);
   lm.eps = d->eps;
+  lm.tags = tag_in(B_H);
   ops.push_back(lm);
   EngOp am;
   memset(&am, 0, sizeof(am));
   am.kind = OP_ARGMAX_REDUCE;
   am.flags = F_WAIT;
+  am.wait_target = 1;  // the lm_head step is the only one that arrives
   am.nseg = 1;
   ops.push_back(am);
+  for (int b = 0; b < 6; ++b) c->writes_per_token[b] = ver[b];
+  c->writes_per_token[B_KV] = 1;
   c->n_ops = (int)ops.size();
   if (cudaMalloc(&c->d_ops, sizeof(EngOp) * ops.size()) != cudaSuccess) {
     (void)cudaGetLastError();
@@ -1474,11 +2046,15 @@ extern "C" int fak_decode_step(fak_decode* c, const int32_t* tok_in, int32_t* to
   P.tok_out = tok_out;
   P.logits = logits;
   P.timeout_ns = c->timeout_ns;
+  P.flip = tag_flip(c);
+  P.pos = c->pos;
   if (c->mode == FAK_DECODE_ONE_LAUNCH) {
     P.sync = c->sync;
     P.n_ops = c->n_ops;
     P.first_wait = 0;
-    return launch_engine(P, c->sms, true, s, c->i8x);
+    const int st = launch_engine(P, c->sms, true, s, c->i8x);
+    if (st == FAK_OK) ++c->token;
+    return st;
   }
   for (int i = 0; i < c->n_ops; ++i) {
     P.ops = c->d_ops + i;
@@ -1487,6 +2063,7 @@ extern "C" int fak_decode_step(fak_decode* c, const int32_t* tok_in, int32_t* to
     int st = launch_engine(P, c->sms, false, s, c->i8x);
     if (st != FAK_OK) return st;
   }
+  ++c->token;
   return FAK_OK;
 }
 
@@ -1498,17 +2075,33 @@ extern "C" int fak_decode_status(fak_decode* c, fak_stream_t stream) {
   e = cudaMemcpy(&v, c->err, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return fak_cuda_status(e);
   cudaMemset(c->err, 0, sizeof(int));
-  if (v != 0) cudaMemset(c->sync, 0, 64);
+  if (v != 0) {
+    // an aborted step leaves the counters and the tagged buffers half-written: start over
+    cudaMemset(c->sync, 0, 64);
+    int st = reset_tags(c, (cudaStream_t)stream);
+    if (st == FAK_OK) st = reset_mixer_state(c, (cudaStream_t)stream);
+    if (st != FAK_OK) return st;
+    e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return fak_cuda_status(e);
+  }
   return v;
 }
 
 extern "C" int fak_decode_read_state(fak_decode* c, int which, float* dst, size_t count, fak_stream_t stream) {
-  if (!c || !dst || (which != 0 && which != 1)) return FAK_ERR_INVALID_ARG;
-  const size_t n = which == 0 ? (size_t)c->desc.d_model : (size_t)2 * c->n_fa * c->desc.fa_kv;
+  if (!c || !dst || which < 0 || which > 2) return FAK_ERR_INVALID_ARG;
+  const size_t n = which == 0 ? (size_t)c->desc.d_model
+                              : (which == 1 ? (size_t)2 * c->n_fa * c->desc.fa_kv : (size_t)c->desc.n_mix);
   if (count != n) return FAK_ERR_SHAPE;
   if (n == 0) return FAK_OK;
-  return fak_cuda_status(
-      cudaMemcpyAsync(dst, which == 0 ? c->h : c->kv, n * sizeof(float), cudaMemcpyDefault, (cudaStream_t)stream));
+  const float* src = which == 0 ? c->h : (which == 1 ? c->kv : (c->mixer ? c->mix : c->t));
+  return fak_cuda_status(cudaMemcpyAsync(dst, src, n * sizeof(float), cudaMemcpyDefault, (cudaStream_t)stream));
+}
+
+extern "C" int fak_decode_reset(fak_decode* c, fak_stream_t stream) {
+  if (!c) return FAK_ERR_INVALID_ARG;
+  int st = reset_tags(c, (cudaStream_t)stream);
+  if (st == FAK_OK) st = reset_mixer_state(c, (cudaStream_t)stream);
+  return st;
 }
 
 extern "C" int fak_decode_launches_per_step(const fak_decode* c) {

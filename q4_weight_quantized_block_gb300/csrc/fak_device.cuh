@@ -117,6 +117,48 @@ FAK_DEV int ld_cg_i(const int* p) {
   return v;
 }
 
+// Strong (relaxed, gpu scope) accesses for values that carry a version tag in
+// their lowest significand bit: they are read from and written to L2, the
+// point of coherence, so a poll that sees the tag it waits for sees the value
+// stored with it (same 32-bit word).
+FAK_DEV float4 ld_relaxed_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+FAK_DEV float ld_relaxed_f(const float* p) {
+  float v;
+  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Stores v rounded to 22 significand bits (to nearest, ties to even: no drift
+// over the many residual updates of a decode token) with the tag in the freed
+// lowest bit; consumers read it back through untag.
+FAK_DEV void st_tagged(float* p, float v, uint32_t tag) {
+  uint32_t b = __float_as_uint(v);
+  b = (b & 1u) ? ((b & 2u) ? b + 1u : b - 1u) : b;
+  b |= tag;
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(b) : "memory");
+}
+
+// The value a tagged word stands for: its tag bit cleared.  Every consumer uses
+// this, so a value does not depend on which tag it was stored with.
+FAK_DEV float untag(float v) { return __uint_as_float(__float_as_uint(v) & ~1u); }
+FAK_DEV float4 untag4(float4 v) { return make_float4(untag(v.x), untag(v.y), untag(v.z), untag(v.w)); }
+
+// Non-zero when any of the eight values lacks the version tag `want`.
+FAK_DEV uint32_t stale8(const float4& a, const float4& b, uint32_t want) {
+  const uint32_t o = (__float_as_uint(a.x) ^ want) | (__float_as_uint(a.y) ^ want) | (__float_as_uint(a.z) ^ want) |
+                     (__float_as_uint(a.w) ^ want) | (__float_as_uint(b.x) ^ want) | (__float_as_uint(b.y) ^ want) |
+                     (__float_as_uint(b.z) ^ want) | (__float_as_uint(b.w) ^ want);
+  return o & 1u;
+}
+
 // named barrier among `count` threads (count a multiple of 32)
 FAK_DEV void named_bar_sync(int id, int count) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory"); }
 

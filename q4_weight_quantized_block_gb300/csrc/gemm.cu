@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int64_t pp = p0 + 32 * ch + j;
-            if (pp < p.P) p.Y[pp * p.N + n] = __uint_as_float(r[j]);
+            if (pp < p.P && n < p.N) p.Y[pp * p.N + n] = __uint_as_float(r[j]);
           }
         }
       }
@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int64_t pp = p0 + c0 + 4 * i + e;
-                if (pp < p.P) p.Y[pp * p.N + n] = o[e];
+                if (pp < p.P && n < p.N) p.Y[pp * p.N + n] = o[e];
               }
             }
           }
@@ -548,7 +548,7 @@ extern "C" int fak_swiglu_bf16(const float* Y1, int64_t P, int64_t half, void* X
 namespace {
 int launch_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, float* Y, __nv_bfloat16* x2,
                 fak_stream_t stream) {
-  if (K < 256 || K % 256 || N < 128 || N % 128 || P < 1 || P > (1LL << 31) - 1 || K > (1LL << 31) - 1)
+  if (K < 256 || K % 256 || N < 1 || N > (1LL << 31) - 1 || P < 1 || P > (1LL << 31) - 1 || K > (1LL << 31) - 1)
     return FAK_ERR_SHAPE;
   if ((reinterpret_cast<uintptr_t>(Wq) & 15) || (reinterpret_cast<uintptr_t>(X) & 15)) return FAK_ERR_ALIGN;
   int sms = 0;
@@ -581,7 +581,7 @@ int launch_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, 
   gp.N = N;
   gp.K = K;
   gp.P = P;
-  gp.n_tiles_n = (int)(N / BM);
+  gp.n_tiles_n = (int)((N + BM - 1) / BM);  // a last partial tile reads zero-filled rows past N, writes none
   gp.n_tiles_p = (int)((P + BN - 1) / BN);
   gp.timeout_ns = 2000000000ull;
   const int tiles = gp.n_tiles_n * gp.n_tiles_p;

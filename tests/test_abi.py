@@ -54,7 +54,7 @@ def test_validation_happens_before_any_device_call(fak):
     assert lib.fak_q4k_gemv_batch(ok_ptr, 16, 256, ok_ptr, 4, ok_ptr + 2, None) == 3
     assert lib.fak_mlp_decode(ok_ptr, ok_ptr, ok_ptr, 256, 512, ok_ptr, 1e-6, ok_ptr, ok_ptr, 16, None) == 2
     assert lib.fak_mlp_decode(ok_ptr, ok_ptr, None, 256, 512, ok_ptr, 1e-6, ok_ptr, ok_ptr, 4096, None) == 1
-    assert lib.fak_q4k_gemm(ok_ptr, 100, 256, ok_ptr, 8, ok_ptr, None) == 2
+    assert lib.fak_q4k_gemm(ok_ptr, 0, 256, ok_ptr, 8, ok_ptr, None) == 2
     assert lib.fak_q4k_gemm(ok_ptr, 128, 256, ok_ptr, 0, ok_ptr, None) == 2
     assert lib.fak_q4k_gemm(ok_ptr, 128, 300, ok_ptr, 8, ok_ptr, None) == 2
     assert lib.fak_q4k_gemm(ok_ptr + 8, 128, 256, ok_ptr, 8, ok_ptr, None) == 3

@@ -49,9 +49,12 @@ def check_gemm(got, ref, a, what):
 
 
 # (640, 8192, 256) and (128, 10496, 64) have few tiles: K is split across CTAs (4 splits of 8
-# super-blocks; 11 + 11 + 11 + 8) and the partial tiles are summed in split order
+# super-blocks; 11 + 11 + 11 + 8) and the partial tiles are summed in split order.  N that is not a
+# multiple of 128 leaves a last partial row tile: (200, 512, 33), the GDN in_proj rows (16480, 5120, 8)
+# and a split-K one (1000, 8192, 64).
 @pytest.mark.parametrize("N,K,P", [(128, 256, 1), (128, 256, 7), (256, 512, 256), (384, 1280, 300),
-                                   (128, 2048, 513), (512, 5120, 64), (640, 8192, 256), (128, 10496, 64)])
+                                   (128, 2048, 513), (512, 5120, 64), (640, 8192, 256), (128, 10496, 64),
+                                   (200, 512, 33), (16480, 5120, 8), (1000, 8192, 64)])
 def test_gemm_small_full_compare(fak, N, K, P):
     w = synth.normal(40, N + K + P, (N, K), 0.02)
     Wg, Wo = fak.fak_q4k_pack(w), oracle.q4k_pack(w)

@@ -494,3 +494,47 @@ def test_gemv_act_i8_exact_arithmetic():
         sabs = sum(abs(wi * xi) for wi, xi in zip(w, xq))
         assert abs(Fraction(y[n]) - exact) <= sabs * Fraction(1, 2 ** 23)
         assert abs(a[n] - float(sabs)) <= float(sabs) * 2 ** -20
+
+
+# ------------------------------------------------------------------ bf16 rounding, prefill forward
+def test_bf16_rne_is_nearest_with_ties_to_even():
+    # hand-decided cases: halfway points go to the even significand
+    assert oracle.bf16_rne(1.0) == 0x3F80
+    assert oracle.bf16_rne(1.0 + 2.0 ** -8) == 0x3F80            # tie between 0x3F80 (even) and 0x3F81
+    assert oracle.bf16_rne(1.0 + 3 * 2.0 ** -8) == 0x3F82        # tie between 0x3F81 and 0x3F82 (even)
+    assert oracle.bf16_rne(-(1.0 + 2.0 ** -8 + 2.0 ** -20)) == 0xBF81
+    assert oracle.bf16_rne(0.0) == 0 and oracle.bf16_rne(-0.0) == 0x8000
+    # random values: no other bfloat16 is closer, and ties pick the even pattern
+    rng = np.random.default_rng(30)
+    xs = (rng.standard_normal(4000) * 10.0 ** rng.integers(-30, 30, 4000)).astype(np.float32)
+    for x in xs:
+        b = oracle.bf16_rne(x)
+        v = oracle.bf16_decode(b)
+        err = abs(float(x) - v)
+        for nb in (b - 1, b + 1):
+            assert err <= abs(float(x) - oracle.bf16_decode(nb & 0xFFFF))
+            if err == abs(float(x) - oracle.bf16_decode(nb & 0xFFFF)):
+                assert b % 2 == 0
+
+
+def test_prefill_forward_equals_layers_one_by_one():
+    D, F, V, n_mix, kv = 256, 512, 300, 256, 256
+    m, layers, lm, emb = _tiny_model()
+    toks = np.array([7, 3, 299, 0, 42])
+    nxt, logits, la, hf = m.prefill_forward(toks)
+    bf = lambda a: synth.to_bf16(np.asarray(a, np.float64).astype(np.float32))
+    P = toks.size
+    h = emb[toks].astype(np.float64)
+    for L in layers:
+        n = np.stack([oracle.rmsnorm(h[p]) for p in range(P)])
+        t, _ = oracle.gemm_q4k(L["w_in"], 512, D, bf(n))
+        h = h + oracle.gemm_q4k(L["w_out"], D, n_mix, bf(t[:, :n_mix]))[0]
+        n = np.stack([oracle.rmsnorm(h[p]) for p in range(P)])
+        g, _ = oracle.gemm_q4k(L["w_gate"], F, D, bf(n))
+        u, _ = oracle.gemm_q4k(L["w_up"], F, D, bf(n))
+        a = oracle.swiglu(g.ravel(), u.ravel()).reshape(P, F)
+        h = h + oracle.gemm_q4k(L["w_down"], D, F, bf(a))[0]
+    assert np.array_equal(h, hf)
+    y, ya = oracle.gemv_q8_0(lm, V, D, oracle.rmsnorm(h[-1]).astype(np.float32))
+    assert np.array_equal(y.astype(np.float32), logits) and np.array_equal(ya, la)
+    assert nxt == int(np.argmax(logits))
