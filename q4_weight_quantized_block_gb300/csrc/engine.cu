@@ -1273,6 +1273,13 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       if (*abort) break;
       const float rn = norm_factor(op, red);
       const EmitInfo E = emit_info(op, rn, P.flip);
+      // split mode with a residual: the combine's first pass gives thread t output row slot t, whose
+      // residual (written by this CTA in an earlier step) is loaded now, under the step's compute
+      float res_pre = 0.0f;
+      if (pl.split && (E.flags & F_RESID) && ctid < pl.ngroups * kSlots) {
+        const int r0 = pl.r_lo + (ctid / kSlots) * g.U, r = ctid % kSlots;
+        if (r < (g.pair ? kSlots / 2 : kSlots) && r < min(g.U, pl.r_hi - r0)) res_pre = resid_load(E, r0 + r);
+      }
       float* part = reinterpret_cast<float*>(smem + kOffPart);
       const int nout = g.pair ? kSlots / 2 : kSlots;  // output rows per group slot set
       float wbv = 0.0f;
@@ -1340,7 +1347,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           const int r0 = pl.r_lo + gi * g.U;
           if (r >= nout || r >= min(g.U, pl.r_hi - r0)) continue;
           const int ru = (r + kSlots / 2) % kSlots;  // the paired up row's slot (SwiGLU steps)
-          const float res = resid_load(E, r0 + r);
+          const float res = t == ctid ? res_pre : resid_load(E, r0 + r);
           const int b0 = gi * g.nslab, e = b0 + g.nslab - 1;
           float v = 0.0f, vu = 0.0f;
           int last = -1;

@@ -88,9 +88,17 @@ def test_swiglu_bf16(fak):
     assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30)
 
 
+def tile_samples(n, tile, rng, extra=8):
+    """One random index in every `tile`-sized block of range(n), plus the ends and a few extra."""
+    picks = [rng.integers(b, min(b + tile, n)) for b in range(0, n, tile)]
+    picks += [0, n - 1] + list(rng.choice(n, extra, replace=False))
+    return np.unique(np.array(picks, dtype=np.int64))
+
+
 @pytest.mark.parametrize("P", [256, 512, 1024])
 def test_prefill_workload_sampled(fak, P):
-    # fused gate||up 34816 x 5120 (seed 2, tensor 0), down 5120 x 17408 (tensor 1), X (tensor 2)
+    # fused gate||up 34816 x 5120 (seed 2, tensor 0), down 5120 x 17408 (tensor 1), X (tensor 2);
+    # sampled outputs cover one row in every 128-row tile and one token in every 256-token tile
     D, F = 5120, 17408
     w1 = synth.normal(2, 0, (2 * F, D), 0.02)
     W1g, W1o = fak.fak_q4k_pack(w1), oracle.q4k_pack(w1)
@@ -99,9 +107,8 @@ def test_prefill_workload_sampled(fak, P):
     Xb = synth.to_bf16(synth.normal(2, 2, (P, D), 1.0))
     Y1 = gemm(fak, dev(W1g), 2 * F, D, dev(Xb.view(np.int16)), P)
     rng = np.random.default_rng(P)
-    rows = np.sort(rng.choice(2 * F, 48, replace=False))
-    rows[0], rows[-1] = 0, 2 * F - 1
-    toks = np.unique(np.concatenate([[0, P - 1], rng.choice(P, 6, replace=False)]))
+    rows = tile_samples(2 * F, 128, rng)
+    toks = tile_samples(P, 256, rng, extra=4)
     Yr, Ar = oracle.gemm_q4k_sample(W1o, 2 * F, D, Xb, rows, toks)
     check_gemm(Y1.cpu().numpy()[np.ix_(toks, rows)], Yr, Ar, "prefill gate||up P=%d" % P)
     # second shape, isolated: down projection on the GPU's own SwiGLU output
@@ -112,9 +119,20 @@ def test_prefill_workload_sampled(fak, P):
     del w2
     Y2 = gemm(fak, dev(W2g), D, F, X2, P)
     X2h = X2.cpu().numpy().view(np.uint16)
-    rows2 = np.sort(rng.choice(D, 48, replace=False))
+    rows2 = tile_samples(D, 128, rng)
     Yr2, Ar2 = oracle.gemm_q4k_sample(W2o, D, F, X2h, rows2, toks)
     check_gemm(Y2.cpu().numpy()[np.ix_(toks, rows2)], Yr2, Ar2, "prefill down P=%d" % P)
+    # second shape, end to end from the oracle's own X2 = bf16(silu(g) * u) for two tokens: the GPU's
+    # down GEMM fed with it meets the GEMM bar, and the GPU's whole pipeline (its own X2) stays
+    # within twice the bar (two bf16 GEMMs in series) of the oracle's whole pipeline
+    t2 = np.array([0, P - 1])
+    Yfull, _ = oracle.gemm_q4k(W1o, 2 * F, D, Xb[t2])
+    x2o = synth.to_bf16(oracle.swiglu(Yfull[:, :F].ravel(), Yfull[:, F:].ravel()).astype(np.float32)).reshape(2, F)
+    Yo2, Ao2 = oracle.gemm_q4k(W2o, D, F, x2o)
+    Yg2 = gemm(fak, dev(W2g), D, F, dev(x2o.view(np.int16)), 2)
+    check_gemm(Yg2.cpu().numpy(), Yo2, Ao2, "prefill down from the oracle's X2, P=%d" % P)
+    check_f32(Y2.cpu().numpy()[t2], Yo2, Ao2, "prefill gate||up -> SwiGLU -> down end to end, P=%d" % P,
+              rel=1e-2, abs_=2e-5, cos_min=0.9999)
 
 
 def interleave_rows(g, u):
