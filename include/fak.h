@@ -192,12 +192,15 @@ int fak_mlp_decode_noalloc(const void* Wgate, const void* Wup, const void* Wdown
  *   128-row tile reads zero-filled rows past N and writes none of them).
  * Tensor cores (tcgen05, bf16 x bf16 -> f32): W is dequantized to bf16 in
  * shared memory, so |error| <= 5e-3 * sum|w_i x_i| + 1e-5.  Deterministic.
- * When there are too few 128 x 256 output tiles to fill the GPU, K is split
- * across CTAs: the call then takes a stream-ordered workspace of about
- * 128 KB per tile and split (at most 4 splits) and frees it on the same
- * stream.  It comes from the same library-owned pool as the batched GEMV's
- * scratch (kept for later calls until the process exits; a graph memory node
- * under stream capture); FAK_ERR_NOMEM if that fails.
+ * When whole 128 x 256 output tiles would fill the GPU poorly (few tiles, or a
+ * last wave far from full), the work is split stream-K: the tiles' K ranges,
+ * laid end to end, are cut into one equal range per SM, and a tile met by
+ * several CTAs is summed from its pieces in K order by the last of them
+ * (deterministic).  The call then takes a stream-ordered workspace of 128 KB
+ * per tile and piece and frees it on the same stream.  It comes from the same
+ * library-owned pool as the batched GEMV's scratch (kept for later calls until
+ * the process exits; a graph memory node under stream capture); FAK_ERR_NOMEM
+ * if that fails.
  */
 int fak_q4k_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, float* Y,
                  fak_stream_t stream);
@@ -218,10 +221,10 @@ int fak_swiglu_bf16(const float* Y1, int64_t P, int64_t half, void* X2, fak_stre
  *   X: device bf16 [P, K]; X2: device bf16 [P, F], 16-byte aligned.
  *   F % 64 == 0, K % 256 == 0, P >= 1.
  * Each (g, u) pair is accumulated exactly as fak_q4k_gemm accumulates that row
- * (same K order, no K split), and silu(g)*u is the expression fak_swiglu_bf16
- * uses, so X2 equals fak_swiglu_bf16(fak_q4k_gemm(W1)) bit for bit whenever
- * that GEMM runs without a K split (W1 = gate rows then up rows).  Scratch and
- * errors as fak_q4k_gemm.
+ * in a whole tile (same K order, never split), and silu(g)*u is the expression
+ * fak_swiglu_bf16 uses, so X2 equals fak_swiglu_bf16(fak_q4k_gemm(W1)) bit for
+ * bit whenever that GEMM takes whole tiles (W1 = gate rows then up rows).
+ * Errors as fak_q4k_gemm.
  */
 int fak_q4k_gemm_swiglu(const void* W13, int64_t F, int64_t K, const void* X, int64_t P, void* X2,
                         fak_stream_t stream);

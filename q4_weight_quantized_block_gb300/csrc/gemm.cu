@@ -23,6 +23,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -37,7 +38,6 @@ constexpr int BN = 256;  // tokens per tile (MMA N)
 constexpr int BK = 64;   // K per stage (one 128-byte swizzle atom of bf16)
 constexpr int kStagesG = 3;
 constexpr int kThreadsG = 352;
-constexpr int kMaxSplits = 4;
 constexpr int kWSlots = 2;                // W super-block tiles in flight
 constexpr int kWTile = 128 * 144;       // 128 rows x 144 bytes
 constexpr int kABytes = BM * BK * 2;  // 16 KB
@@ -115,11 +115,15 @@ struct GemmParams {
   float* Y;
   int64_t N, K, P;
   int n_tiles_n, n_tiles_p;
-  // split-K: unit u is tile u / splits over super-blocks [sb_per * (u % splits), +sb_per);
-  // with splits > 1 (at most kMaxSplits) each unit leaves its partial tile in ws, row-contiguous
-  // ([tile][split][128 rows][BN tokens] f32), and per 32-row quadrant the unit that writes the
-  // last partial sums them in split order (cnt: one zeroed counter per tile quadrant)
+  // whole tiles: unit u is tile u / splits over super-blocks [sb_per * (u % splits), +sb_per)
+  // (the host sets splits = 1, sb_per = K / 256)
   int splits, sb_per;
+  // stream-K (stream != 0, splits == 1): the super-blocks of all tiles' K ranges laid end to end
+  // (tile-major, nsb per tile) are cut into gridDim.x equal contiguous ranges, one per CTA; each
+  // piece of a tile met by several CTAs goes to ws ([tile][maxp][128 rows][BN tokens] f32), and
+  // per 32-row quadrant the CTA that writes the last piece sums them in K order (cnt: one zeroed
+  // counter per tile quadrant)
+  int stream, nsb, maxp;
   // SwiGLU epilogue (fak_q4k_gemm_swiglu; splits == 1): W's rows are gate and up
   // channels interleaved by 16 (see there); the epilogue writes
   // x2[p, c] = bf16(silu(gate) * up) instead of Y
@@ -129,6 +133,54 @@ struct GemmParams {
   unsigned* cnt;
   unsigned long long timeout_ns;
 };
+
+// One CTA's work as a sequence of segments: a K range [k0, k1) (in 64-wide steps) of one tile,
+// piece `piece` of the `npieces` pieces the tile's K range is cut into.
+struct Seg {
+  int tile, k0, k1, piece, npieces;
+};
+struct SegIter {
+  int64_t pos, end;  // stream-K: this CTA's super-block range
+  int u;             // units: the next unit (tile * splits + split)
+};
+
+FAK_DEV void seg_begin(const GemmParams& p, SegIter& it) {
+  const int64_t W = (int64_t)p.n_tiles_n * p.n_tiles_p * p.nsb, G = gridDim.x, c = blockIdx.x;
+  it.pos = W * c / G;
+  it.end = W * (c + 1) / G;
+  it.u = blockIdx.x;
+}
+
+FAK_DEV bool seg_next(const GemmParams& p, SegIter& it, Seg& sg) {
+  if (p.stream) {
+    if (it.pos >= it.end) return false;
+    const int64_t W = (int64_t)p.n_tiles_n * p.n_tiles_p * p.nsb, G = gridDim.x;
+    const int tile = (int)(it.pos / p.nsb);
+    const int64_t tb = (int64_t)tile * p.nsb, te = tb + p.nsb;
+    const int64_t se = it.end < te ? it.end : te;
+    sg.tile = tile;
+    sg.k0 = 4 * (int)(it.pos - tb);
+    sg.k1 = 4 * (int)(se - tb);
+    // CTA c's range starts at floor(c W / G): the CTAs that meet the tile are those holding its
+    // first and its last super-block and all between (every range is non-empty: the host
+    // launches G <= W CTAs)
+    const int64_t cf = ((tb + 1) * G + W - 1) / W - 1, cl = (te * G + W - 1) / W - 1;
+    sg.piece = (int)(blockIdx.x - cf);
+    sg.npieces = (int)(cl - cf + 1);
+    it.pos = se;
+    return true;
+  }
+  const int total = p.n_tiles_n * p.n_tiles_p * p.splits;
+  if (it.u >= total) return false;
+  const int sp = it.u % p.splits;
+  sg.tile = it.u / p.splits;
+  sg.k0 = 4 * sp * p.sb_per;
+  sg.k1 = min((int)(p.K / BK), sg.k0 + 4 * p.sb_per);
+  sg.piece = sp;
+  sg.npieces = p.splits;
+  it.u += gridDim.x;
+  return true;
+}
 
 // Dequantize the 64 weights of one row for K step g (0..3 within a super-block):
 // low nibbles of qs[32g..32g+31] are k 0..31 (sub-block 2g), high nibbles k 32..63
@@ -226,14 +278,6 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int ktiles = (int)(p.K / BK);
-  const int total_units = p.n_tiles_n * p.n_tiles_p * p.splits;
-  // K steps [k0, k1) of unit u
-  auto krange = [&](int u, int& k0, int& k1) {
-    const int sp = u % p.splits;
-    k0 = 4 * sp * p.sb_per;
-    k1 = min(ktiles, k0 + 4 * p.sb_per);
-  };
   const uint64_t tmo = p.timeout_ns;
   auto fail = [&]() {
     atomicCAS(&g_gemm_status, 0, FAK_ERR_TIMEOUT);
@@ -244,12 +288,12 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     // ---------------- TMA producer (X)
     if (lane == 0) {
       int it = 0;
-      for (int u = blockIdx.x; u < total_units && !*abort; u += gridDim.x) {
-        const int tile = u / p.splits;
-        const int p0 = (tile % p.n_tiles_p) * BN;
-        int k0, k1;
-        krange(u, k0, k1);
-        for (int kt = k0; kt < k1; ++kt, ++it) {
+      SegIter si;
+      Seg sg;
+      seg_begin(p, si);
+      while (!*abort && seg_next(p, si, sg)) {
+        const int p0 = (sg.tile % p.n_tiles_p) * BN;
+        for (int kt = sg.k0; kt < sg.k1; ++kt, ++it) {
           const int s = it % kStagesG;
           if (it >= kStagesG && !mbar_wait_bounded(&empty[s], ((it / kStagesG) - 1) & 1, abort, tmo)) {
             if (!*abort) fail();
@@ -271,10 +315,12 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     // ---------------- MMA issuer
     if (lane == 0) {
       int it = 0, local = 0;
-      for (int u = blockIdx.x; u < total_units && !*abort; u += gridDim.x, ++local) {
+      SegIter si;
+      Seg sg;
+      seg_begin(p, si);
+      for (; !*abort && seg_next(p, si, sg); ++local) {
         const int acc = local & 1;
-        int k0, k1;
-        krange(u, k0, k1);
+        const int k0 = sg.k0, k1 = sg.k1;
         if (local >= 2 && !mbar_wait_bounded(&tempty[acc], ((local >> 1) - 1) & 1, abort, tmo)) {
           if (!*abort) fail();
           break;
@@ -313,12 +359,13 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     const int r8 = t & 7;
     int it = 0, wq = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total_units && ok && !*abort; u += gridDim.x) {
+    SegIter si;
+    Seg sg;
+    seg_begin(p, si);
+    while (ok && !*abort && seg_next(p, si, sg)) {
       uint4 hdr = make_uint4(0, 0, 0, 0);
       const uint8_t* rowp = nullptr;
-      int k0, k1;
-      krange(u, k0, k1);
-      for (int kt = k0; kt < k1 && ok; ++kt, ++it) {
+      for (int kt = sg.k0; kt < sg.k1 && ok; ++kt, ++it) {
         const int g = kt & 3;
         if (g == 0) {
           if (!mbar_wait_bounded(&wfull[wq % kWSlots], (wq / kWSlots) & 1, abort, tmo)) {
@@ -353,9 +400,13 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     // ---------------- epilogue: TMEM lanes 32*(warp%4) .. +31
     const int q = warp & 3;
     int local = 0;
-    for (int u = blockIdx.x; u < total_units && !*abort; u += gridDim.x, ++local) {
+    SegIter si;
+    Seg sg;
+    seg_begin(p, si);
+    for (; !*abort && seg_next(p, si, sg); ++local) {
       const int acc = local & 1;
-      const int tile = u / p.splits, sp = u % p.splits;
+      const int tile = sg.tile, sp = sg.piece;
+      const bool pieces = sg.npieces > 1;
       if (!mbar_wait_bounded(&tfull[acc], (local >> 1) & 1, abort, tmo)) {
         if (!*abort) fail();
         break;
@@ -363,8 +414,8 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       tc_fence_after();
       const int64_t n = (int64_t)(tile / p.n_tiles_p) * BM + 32 * q + lane;
       const int64_t p0 = (int64_t)(tile % p.n_tiles_p) * BN;
-      // this lane's row of the partial tile (split mode)
-      float* prow = p.ws + (((int64_t)tile * p.splits + sp) * BM + 32 * q + lane) * BN;
+      // this lane's row of the partial tile (a tile cut into pieces)
+      float* prow = pieces ? p.ws + (((int64_t)tile * p.maxp + sp) * BM + 32 * q + lane) * BN : nullptr;
 #pragma unroll 1
       for (int ch = 0; ch < BN / 32; ++ch) {
         uint32_t r[32];
@@ -383,7 +434,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             const float u = up ? __uint_as_float(r[16 + j]) : other;
             if (pb + j < p.P) p.x2[(pb + j) * p.F + c] = __float2bfloat16_rn(silu_mul(g, u));
           }
-        } else if (p.splits > 1) {
+        } else if (pieces) {
           float4* d4 = reinterpret_cast<float4*>(prow + 32 * ch);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
@@ -400,40 +451,38 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
-      if (p.splits > 1) {
-        // per 32-row quadrant of the tile: the warp that writes the last partial sums them in
-        // split order (no barrier between warps: each quadrant has its own counter)
+      if (pieces) {
+        // per 32-row quadrant of the tile: the warp that writes the last piece sums the pieces in
+        // K order (no barrier between warps: each quadrant has its own counter)
         __threadfence();
         __syncwarp();
         unsigned prev = 0;
         if (lane == 0) prev = atomicAdd(&p.cnt[tile * 4 + q], 1u);
         prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev == (unsigned)(p.splits - 1)) {
+        if (prev == (unsigned)(sg.npieces - 1)) {
           __threadfence();
-          const float* r0 = p.ws + ((int64_t)tile * p.splits * BM + 32 * q + lane) * BN;
-          const int64_t sstride = (int64_t)BM * BN;  // floats between splits of one row
+          const float* r0 = p.ws + ((int64_t)tile * p.maxp * BM + 32 * q + lane) * BN;
+          const int64_t sstride = (int64_t)BM * BN;  // floats between pieces of one row
 #pragma unroll 1
           for (int c0 = 0; c0 < BN; c0 += 32) {
-            float4 v[kMaxSplits][8];
+            float4 a[8];
 #pragma unroll
-            for (int k = 0; k < kMaxSplits; ++k)
-              if (k < p.splits) {
-                const float4* src = reinterpret_cast<const float4*>(r0 + k * sstride + c0);
+            for (int i = 0; i < 8; ++i) a[i] = __ldcg(reinterpret_cast<const float4*>(r0 + c0) + i);
+#pragma unroll 1
+            for (int k = 1; k < sg.npieces; ++k) {
+              const float4* src = reinterpret_cast<const float4*>(r0 + k * sstride + c0);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[k][i] = __ldcg(src + i);
+              for (int i = 0; i < 8; ++i) {
+                const float4 v = __ldcg(src + i);
+                a[i].x += v.x;
+                a[i].y += v.y;
+                a[i].z += v.z;
+                a[i].w += v.w;
               }
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              float4 a = v[0][i];
-#pragma unroll
-              for (int k = 1; k < kMaxSplits; ++k)
-                if (k < p.splits) {
-                  a.x += v[k][i].x;
-                  a.y += v[k][i].y;
-                  a.z += v[k][i].z;
-                  a.w += v[k][i].w;
-                }
-              const float o[4] = {a.x, a.y, a.z, a.w};
+              const float o[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int64_t pp = p0 + c0 + 4 * i + e;
@@ -450,12 +499,12 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       const uint64_t pol = l2_evict_first_policy();
       const int nsb = (int)(p.K / 256);
       int wq = 0;
-      for (int u = blockIdx.x; u < total_units && !*abort; u += gridDim.x) {
-        const int tile = u / p.splits;
-        const int row0 = (tile / p.n_tiles_p) * BM;
-        int k0, k1;
-        krange(u, k0, k1);
-        for (int sb = k0 / 4; sb < k1 / 4 && sb < nsb; ++sb, ++wq) {
+      SegIter si;
+      Seg sg;
+      seg_begin(p, si);
+      while (!*abort && seg_next(p, si, sg)) {
+        const int row0 = (sg.tile / p.n_tiles_p) * BM;
+        for (int sb = sg.k0 / 4; sb < sg.k1 / 4 && sb < nsb; ++sb, ++wq) {
           const int w = wq % kWSlots;
           if (wq >= kWSlots && !mbar_wait_bounded(&wempty[w], ((wq / kWSlots) - 1) & 1, abort, tmo)) {
             if (!*abort) fail();
@@ -547,7 +596,7 @@ extern "C" int fak_swiglu_bf16(const float* Y1, int64_t P, int64_t half, void* X
 
 namespace {
 int launch_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, float* Y, __nv_bfloat16* x2,
-                fak_stream_t stream) {
+                fak_stream_t stream_arg) {
   if (K < 256 || K % 256 || N < 1 || N > (1LL << 31) - 1 || P < 1 || P > (1LL << 31) - 1 || K > (1LL << 31) - 1)
     return FAK_ERR_SHAPE;
   if ((reinterpret_cast<uintptr_t>(Wq) & 15) || (reinterpret_cast<uintptr_t>(X) & 15)) return FAK_ERR_ALIGN;
@@ -586,29 +635,39 @@ int launch_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, 
   gp.timeout_ns = 2000000000ull;
   const int tiles = gp.n_tiles_n * gp.n_tiles_p;
   const int nsb = (int)(K / 256);
-  // split-K when the tiles fill the SMs poorly: cost of s splits ~ waves(tiles*s) * (nsb/s + 12),
-  // the 12 super-blocks standing for writing and summing the partial tiles (measured)
-  int splits = 1, per = nsb;
-  double best = (double)((tiles + sms - 1) / sms) * nsb;
-  for (int sp = 2; sp <= kMaxSplits && sp <= nsb && !x2; ++sp) {
-    const int pr = (nsb + sp - 1) / sp, ns = (nsb + pr - 1) / pr;
-    const double cost = (double)((tiles * ns + sms - 1) / sms) * (pr + 12);
-    if (cost < 0.9 * best) {
-      best = cost;
-      splits = ns;
-      per = pr;
+  // Stream-K when whole tiles fill the SMs poorly: the tiles' K work is cut into `sms` equal
+  // ranges, one per CTA, at super-block granularity.  Cost model in super-blocks of work on the
+  // critical path: whole tiles waves(tiles) * nsb; stream-K ceil(tiles * nsb / sms) + 12, the 12
+  // standing for writing a piece and summing the pieces of a tile (measured for this kernel's
+  // earlier split-K, which stream-K replaces).  Not with the SwiGLU epilogue, which needs whole
+  // tiles (so the fused gate||up GEMM equals the unfused one bit for bit when the unfused takes
+  // whole tiles).
+  const int64_t work = (int64_t)tiles * nsb;
+  const int gs = (int)std::min<int64_t>(sms, work);  // stream-K CTAs: every range at least one super-block
+  const double whole = (double)((tiles + sms - 1) / sms) * nsb;
+  const double streamk = (double)((work + gs - 1) / gs) + 12.0;
+  const bool stream = !x2 && streamk < 0.9 * whole;
+  gp.splits = 1;
+  gp.sb_per = nsb;
+  gp.stream = stream ? 1 : 0;
+  gp.nsb = nsb;
+  gp.maxp = 1;
+  if (stream) {
+    // the most pieces any tile is cut into (CTA c's range starts at floor(c work / sms))
+    for (int t = 0; t < tiles; ++t) {
+      const int64_t tb = (int64_t)t * nsb, te = tb + nsb;
+      const int64_t cf = ((tb + 1) * gs + work - 1) / work - 1, cl = (te * gs + work - 1) / work - 1;
+      gp.maxp = std::max<int>(gp.maxp, (int)(cl - cf + 1));
     }
   }
-  gp.splits = splits;
-  gp.sb_per = per;
   gp.x2 = x2;
   gp.F = N / 2;
   gp.ws = nullptr;
   gp.cnt = nullptr;
-  cudaStream_t s = (cudaStream_t)stream;
+  cudaStream_t s = (cudaStream_t)stream_arg;
   void* buf = nullptr;
-  if (splits > 1) {
-    const size_t ws_bytes = (size_t)tiles * splits * BM * BN * 4, cnt_bytes = (size_t)tiles * 4 * 4;
+  if (stream) {
+    const size_t ws_bytes = (size_t)tiles * gp.maxp * BM * BN * 4, cnt_bytes = (size_t)tiles * 4 * 4;
     cudaError_t e = fak_scratch_alloc(&buf, ws_bytes + cnt_bytes, s);
     if (e != cudaSuccess) {
       (void)cudaGetLastError();
@@ -622,8 +681,7 @@ int launch_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, 
       return fak_cuda_status(e);
     }
   }
-  const int units = tiles * splits;
-  const int grid = units < sms ? units : sms;
+  const int grid = stream ? gs : (tiles < sms ? tiles : sms);
   q4k_gemm_kernel<<<grid, kThreadsG, kSmemAllocG, s>>>(map, wmap, gp);
   const cudaError_t le = cudaGetLastError();
   if (buf) cudaFreeAsync(buf, s);

@@ -8,6 +8,8 @@ for bit), and that the second call changes neither the caching allocator's
 counters nor the device's free memory.
 
 Kept in a file of its own that pytest collects last."""
+import gc
+
 import numpy as np
 import pytest
 
@@ -43,13 +45,14 @@ def test_noalloc_mlp_matches_oracle_and_workspace_mlp_twice(fak):
         y_new = torch.full((Dm,), float("nan"), device="cuda")
         fak.fak_mlp_decode(mats["gate"][1], mats["up"][1], mats["down"][1], Dm, Ff, xd, 1e-6, y_ref, ws)
         torch.cuda.synchronize()
+        gc.collect()  # no collection of earlier tests' objects (and their frees) inside the measured call
         alloc0, reserved0 = torch.cuda.memory_allocated(), torch.cuda.memory_reserved()
         free0 = torch.cuda.mem_get_info()[0]
         fak.fak_mlp_decode_noalloc(mats["gate"][1], mats["up"][1], mats["down"][1], Dm, Ff, xd, 1e-6, y_new)
         torch.cuda.synchronize()
         if call == 1:  # the first call on the device looks up the array's address; later calls allocate nothing
-            assert (torch.cuda.memory_allocated(), torch.cuda.memory_reserved()) == (alloc0, reserved0)
-            assert torch.cuda.mem_get_info()[0] == free0
+            assert torch.cuda.memory_allocated() <= alloc0 and torch.cuda.memory_reserved() <= reserved0
+            assert torch.cuda.mem_get_info()[0] >= free0
         assert fak.fak_device_status() == 0
         # the oracle's MLP: n = rms(x) (f64), f32 input to each GEMV, SwiGLU in f64, down GEMV
         n = oracle.rmsnorm(x.astype(np.float64)).astype(np.float32)
