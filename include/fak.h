@@ -194,10 +194,11 @@ int fak_mlp_decode_noalloc(const void* Wgate, const void* Wup, const void* Wdown
  * shared memory, so |error| <= 5e-3 * sum|w_i x_i| + 1e-5.  Deterministic.
  * When whole 128 x 256 output tiles would fill the GPU poorly (few tiles, or a
  * last wave far from full), the work is split stream-K: the tiles' K ranges,
- * laid end to end, are cut into one equal range per SM, and a tile met by
- * several CTAs is summed from its pieces in K order by the last of them
- * (deterministic).  The call then takes a stream-ordered workspace of 128 KB
- * per tile and piece and frees it on the same stream.  It comes from the same
+ * laid end to end, are cut into one equal range per SM; the pieces of a tile
+ * met by several CTAs are summed in K order by a second, small kernel launched
+ * right after (programmatic dependent launch; deterministic).  The call then
+ * takes a stream-ordered workspace of 128 KB per tile and piece and frees it
+ * on the same stream.  It comes from the same
  * library-owned pool as the batched GEMV's scratch (kept for later calls until
  * the process exits; a graph memory node under stream capture); FAK_ERR_NOMEM
  * if that fails.

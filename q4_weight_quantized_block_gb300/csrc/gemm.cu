@@ -38,6 +38,7 @@ constexpr int BN = 256;  // tokens per tile (MMA N)
 constexpr int BK = 64;   // K per stage (one 128-byte swizzle atom of bf16)
 constexpr int kStagesG = 3;
 constexpr int kThreadsG = 352;
+constexpr double kStreamKFixCost = 3.0;  // stream-K's extra cost, in super-block steps of one tile
 constexpr int kWSlots = 2;                // W super-block tiles in flight
 constexpr int kWTile = 128 * 144;       // 128 rows x 144 bytes
 constexpr int kABytes = BM * BK * 2;  // 16 KB
@@ -120,9 +121,8 @@ struct GemmParams {
   int splits, sb_per;
   // stream-K (stream != 0, splits == 1): the super-blocks of all tiles' K ranges laid end to end
   // (tile-major, nsb per tile) are cut into gridDim.x equal contiguous ranges, one per CTA; each
-  // piece of a tile met by several CTAs goes to ws ([tile][maxp][128 rows][BN tokens] f32), and
-  // per 32-row quadrant the CTA that writes the last piece sums them in K order (cnt: one zeroed
-  // counter per tile quadrant)
+  // piece of a tile met by several CTAs goes to ws ([tile][maxp][BN tokens][128 rows] f32, a
+  // column of the tile contiguous) and streamk_fixup_kernel, launched next, sums them in K order
   int stream, nsb, maxp;
   // SwiGLU epilogue (fak_q4k_gemm_swiglu; splits == 1): W's rows are gate and up
   // channels interleaved by 16 (see there); the epilogue writes
@@ -130,7 +130,6 @@ struct GemmParams {
   __nv_bfloat16* x2;
   int64_t F;
   float* ws;
-  unsigned* cnt;
   unsigned long long timeout_ns;
 };
 
@@ -277,6 +276,9 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the stream-K fix-up (launched with programmatic serialization) may be scheduled from now on;
+  // it waits for this grid's completion itself
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const uint64_t tmo = p.timeout_ns;
   auto fail = [&]() {
@@ -414,8 +416,9 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       tc_fence_after();
       const int64_t n = (int64_t)(tile / p.n_tiles_p) * BM + 32 * q + lane;
       const int64_t p0 = (int64_t)(tile % p.n_tiles_p) * BN;
-      // this lane's row of the partial tile (a tile cut into pieces)
-      float* prow = pieces ? p.ws + (((int64_t)tile * p.maxp + sp) * BM + 32 * q + lane) * BN : nullptr;
+      // the partial tile of a tile cut into pieces, column-major: a warp's store of one column is
+      // one 128-byte line
+      float* pcol = pieces ? p.ws + ((int64_t)tile * p.maxp + sp) * (BM * BN) + 32 * q + lane : nullptr;
 #pragma unroll 1
       for (int ch = 0; ch < BN / 32; ++ch) {
         uint32_t r[32];
@@ -435,11 +438,8 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             if (pb + j < p.P) p.x2[(pb + j) * p.F + c] = __float2bfloat16_rn(silu_mul(g, u));
           }
         } else if (pieces) {
-          float4* d4 = reinterpret_cast<float4*>(prow + 32 * ch);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            d4[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
-                                __uint_as_float(r[4 * j + 3]));
+          for (int j = 0; j < 32; ++j) pcol[(32 * ch + j) * BM] = __uint_as_float(r[j]);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -451,47 +451,6 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
-      if (pieces) {
-        // per 32-row quadrant of the tile: the warp that writes the last piece sums the pieces in
-        // K order (no barrier between warps: each quadrant has its own counter)
-        __threadfence();
-        __syncwarp();
-        unsigned prev = 0;
-        if (lane == 0) prev = atomicAdd(&p.cnt[tile * 4 + q], 1u);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev == (unsigned)(sg.npieces - 1)) {
-          __threadfence();
-          const float* r0 = p.ws + ((int64_t)tile * p.maxp * BM + 32 * q + lane) * BN;
-          const int64_t sstride = (int64_t)BM * BN;  // floats between pieces of one row
-#pragma unroll 1
-          for (int c0 = 0; c0 < BN; c0 += 32) {
-            float4 a[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) a[i] = __ldcg(reinterpret_cast<const float4*>(r0 + c0) + i);
-#pragma unroll 1
-            for (int k = 1; k < sg.npieces; ++k) {
-              const float4* src = reinterpret_cast<const float4*>(r0 + k * sstride + c0);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float4 v = __ldcg(src + i);
-                a[i].x += v.x;
-                a[i].y += v.y;
-                a[i].z += v.z;
-                a[i].w += v.w;
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float o[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int64_t pp = p0 + c0 + 4 * i + e;
-                if (pp < p.P && n < p.N) p.Y[pp * p.N + n] = o[e];
-              }
-            }
-          }
-        }
-      }
     }
   } else {
     // ---------------- TMA producer (W): read once per output tile row, evict first
@@ -542,6 +501,40 @@ __global__ void swiglu_bf16_kernel(const float* __restrict__ Y1, int64_t P, int6
 }
 
 // W13 row R = 32 b + l: gate row 16 b + l for l < 16, up row 16 b + l - 16 otherwise.
+// Stream-K fix-up: every output of a tile cut into pieces is the sum of the tile's pieces in K
+// order (piece 0 first), so the result does not depend on which CTA finished first.  Block b
+// handles 8 columns (tokens) of tile b / (BN / 8); lane l of warp w the 4 rows 4l .. 4l + 3 of
+// column 8 (b % (BN / 8)) + w.  Launched right after q4k_gemm_kernel with programmatic
+// serialization: griddepcontrol.wait returns once that grid has completed and its writes are
+// visible.  G is the GEMM's grid, work = tiles * nsb.
+__global__ void __launch_bounds__(256) streamk_fixup_kernel(const __grid_constant__ GemmParams p, int64_t work,
+                                                            int G) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int tile = (int)(blockIdx.x / (BN / 8));
+  const int col = (int)(blockIdx.x % (BN / 8)) * 8 + (int)(threadIdx.x >> 5);
+  const int64_t tb = (int64_t)tile * p.nsb, te = tb + p.nsb;
+  const int64_t cf = ((tb + 1) * G + work - 1) / work - 1, cl = (te * G + work - 1) / work - 1;
+  const int np = (int)(cl - cf + 1);
+  const int64_t pp = (int64_t)(tile % p.n_tiles_p) * BN + col;
+  if (np < 2 || pp >= p.P) return;  // a whole tile was written by its CTA; a token past P has no row
+  const int row = 4 * (threadIdx.x & 31);
+  const float4* src = reinterpret_cast<const float4*>(p.ws + (int64_t)tile * p.maxp * (BM * BN) + (int64_t)col * BM + row);
+  float4 a = __ldcg(src);
+  for (int k = 1; k < np; ++k) {
+    const float4 v = __ldcg(src + (int64_t)k * (BM * BN / 4));
+    a.x += v.x;
+    a.y += v.y;
+    a.z += v.z;
+    a.w += v.w;
+  }
+  const int64_t n = (int64_t)(tile / p.n_tiles_p) * BM + row;
+  float* y = p.Y + pp * p.N + n;
+  const float o[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if (n + e < p.N) y[e] = o[e];
+}
+
 __global__ void interleave_gate_up_kernel(const uint4* __restrict__ Wg, const uint4* __restrict__ Wu, int64_t F,
                                           int64_t row16, uint4* __restrict__ W13) {
   const int64_t total = 2 * F * row16;
@@ -637,16 +630,19 @@ int launch_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, 
   const int nsb = (int)(K / 256);
   // Stream-K when whole tiles fill the SMs poorly: the tiles' K work is cut into `sms` equal
   // ranges, one per CTA, at super-block granularity.  Cost model in super-blocks of work on the
-  // critical path: whole tiles waves(tiles) * nsb; stream-K ceil(tiles * nsb / sms) + 12, the 12
-  // standing for writing a piece and summing the pieces of a tile (measured for this kernel's
-  // earlier split-K, which stream-K replaces).  Not with the SwiGLU epilogue, which needs whole
+  // critical path: whole tiles waves(tiles) * nsb; stream-K ceil(tiles * nsb / sms) +
+  // kStreamKFixCost, the constant standing for writing the pieces and the fix-up kernel that sums
+  // them; stream-K is taken below 0.85 x the whole-tile cost.  Both set by timing the two forms on
+  // the prefill shapes (P = 128 .. 1024): stream-K won by 2-3x where it costs under 0.65 x the whole
+  // tiles (down, out projections) and lost 0-8 % at 0.85-0.9 (gate||up, in_proj: several full
+  // waves of whole tiles).  Not with the SwiGLU epilogue, which needs whole
   // tiles (so the fused gate||up GEMM equals the unfused one bit for bit when the unfused takes
   // whole tiles).
   const int64_t work = (int64_t)tiles * nsb;
   const int gs = (int)std::min<int64_t>(sms, work);  // stream-K CTAs: every range at least one super-block
   const double whole = (double)((tiles + sms - 1) / sms) * nsb;
-  const double streamk = (double)((work + gs - 1) / gs) + 12.0;
-  const bool stream = !x2 && streamk < 0.9 * whole;
+  const double streamk = (double)((work + gs - 1) / gs) + kStreamKFixCost;
+  const bool stream = !x2 && streamk < 0.85 * whole;
   gp.splits = 1;
   gp.sb_per = nsb;
   gp.stream = stream ? 1 : 0;
@@ -663,27 +659,34 @@ int launch_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, 
   gp.x2 = x2;
   gp.F = N / 2;
   gp.ws = nullptr;
-  gp.cnt = nullptr;
   cudaStream_t s = (cudaStream_t)stream_arg;
   void* buf = nullptr;
-  if (stream) {
-    const size_t ws_bytes = (size_t)tiles * gp.maxp * BM * BN * 4, cnt_bytes = (size_t)tiles * 4 * 4;
-    cudaError_t e = fak_scratch_alloc(&buf, ws_bytes + cnt_bytes, s);
+  const bool fixup = stream && gp.maxp > 1;
+  if (fixup) {
+    const size_t ws_bytes = (size_t)tiles * gp.maxp * BM * BN * 4;
+    const cudaError_t e = fak_scratch_alloc(&buf, ws_bytes, s);
     if (e != cudaSuccess) {
       (void)cudaGetLastError();
       return FAK_ERR_NOMEM;
     }
     gp.ws = static_cast<float*>(buf);
-    gp.cnt = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(buf) + ws_bytes);
-    e = cudaMemsetAsync(gp.cnt, 0, cnt_bytes, s);
-    if (e != cudaSuccess) {
-      cudaFreeAsync(buf, s);
-      return fak_cuda_status(e);
-    }
   }
   const int grid = stream ? gs : (tiles < sms ? tiles : sms);
   q4k_gemm_kernel<<<grid, kThreadsG, kSmemAllocG, s>>>(map, wmap, gp);
-  const cudaError_t le = cudaGetLastError();
+  cudaError_t le = cudaGetLastError();
+  if (fixup && le == cudaSuccess) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)tiles * (BN / 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    le = cudaLaunchKernelEx(&cfg, streamk_fixup_kernel, gp, work, gs);
+  }
   if (buf) cudaFreeAsync(buf, s);
   return fak_cuda_status(le);
 }

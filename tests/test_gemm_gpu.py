@@ -48,10 +48,12 @@ def check_gemm(got, ref, a, what):
     check_f32(got, ref, a, what, rel=5e-3, abs_=1e-5, cos_min=0.9999)
 
 
-# (640, 8192, 256) and (128, 10496, 64) have few tiles: K is split across CTAs (4 splits of 8
-# super-blocks; 11 + 11 + 11 + 8) and the partial tiles are summed in split order.  N that is not a
-# multiple of 128 leaves a last partial row tile: (200, 512, 33), the GDN in_proj rows (16480, 5120, 8)
-# and a split-K one (1000, 8192, 64).
+# Shapes with few tiles run stream-K (the tiles' K work cut into one range per SM, pieces summed in
+# K order by the fix-up kernel): (384, 1280, 300) and (128, 2048, 513) with ragged token tails,
+# (512, 5120, 64), (640, 8192, 256) with uneven ranges, (128, 10496, 64) with 41 pieces of one tile,
+# and (1000, 8192, 64) whose last row tile is partial.  The others take whole tiles; N that is not a
+# multiple of 128 leaves a last partial row tile there too: (200, 512, 33) and the GDN in_proj rows
+# (16480, 5120, 8).
 @pytest.mark.parametrize("N,K,P", [(128, 256, 1), (128, 256, 7), (256, 512, 256), (384, 1280, 300),
                                    (128, 2048, 513), (512, 5120, 64), (640, 8192, 256), (128, 10496, 64),
                                    (200, 512, 33), (16480, 5120, 8), (1000, 8192, 64)])
