@@ -22,12 +22,14 @@
 //               chunks of [hi; lo] (128-byte swizzle), plus S and 2^-e of the
 //               super-block (bulk copies)
 //   warps 2-9   dequant sc*q to fp16 straight into TMEM (the MMA's A operand;
-//               thread = row, warp pairs split K), then the epilogue of the
-//               previous super-block (warp pairs split the input rows)
+//               thread = row, the two warps of a TMEM lane quadrant take one K
+//               half each), then the epilogue of an earlier super-block (the
+//               same two warps split the input rows)
 //   warp 10     TMEM owner and MMA issuer: 16 x tcgen05.mma M128 N(2 MP) K16
 //               per super-block, A from TMEM, B from shared memory
-// TMEM: two A buffers (cols 0, 128) and two accumulators (cols 256, 384), so
-// dequant, MMA and epilogue of consecutive super-blocks overlap.  Every wait
+// TMEM: kNBuf A buffers (128 columns each) and as many accumulators, so
+// dequant, MMA and epilogue of consecutive super-blocks overlap (three of each
+// for up to 16 input rows, two above).  Every wait
 // is bounded; on a timeout the kernel records FAK_ERR_TIMEOUT, lets what it
 // issued land, frees TMEM and returns.
 //
@@ -54,9 +56,11 @@ constexpr int kWStages = 4;              // W super-block tiles in flight
 constexpr int kWTileBytes = kBM * 144;   // 18432
 constexpr int kSIStages = 8;             // S / 2^-e records in flight
 constexpr int kBRingBytes = 131072;      // x-part ring
-constexpr int kThreadsB = 352;
+constexpr int kKParts = 2;                    // dequant warps per TMEM lane quadrant, each 256 / kKParts of K
+constexpr int kDqWarps = 4 * kKParts;         // dequant + epilogue warps
+constexpr int kMmaWarp = 2 + kDqWarps;        // TMEM owner and MMA issuer
+constexpr int kThreadsB = 32 * (kMmaWarp + 1);
 constexpr uint32_t kTmemColsB = 512;
-constexpr uint32_t kAccCol = 256;
 
 template <int MP>
 struct BCfg {
@@ -70,7 +74,15 @@ struct BCfg {
   static constexpr int kOffBar = kOffSI + kSIStages * kSIBytes;
   static constexpr int kSmem = kOffBar + 1024;
   static constexpr int kSmemAlloc = kSmem + 1024;
-  static constexpr int kMh = MP / 2;  // input rows per epilogue warp
+  static constexpr int kMq = MP / kKParts;  // input rows per epilogue warp
+  // Super-blocks in flight between dequant, MMA and epilogue: kNBuf A buffers in TMEM (128
+  // columns each) and as many accumulators (kAccW columns each, >= 2 MP); the epilogue runs
+  // kNBuf - 1 super-blocks behind the dequant, so a super-block's MMAs have that long to finish.
+  static constexpr int kNBuf = MP <= 16 ? 3 : 2;
+  static constexpr int kLag = kNBuf - 1;
+  static constexpr uint32_t kAccCol = 128u * kNBuf;
+  static constexpr uint32_t kAccW = MP <= 16 ? 32u : 128u;
+  static_assert(kAccCol + kNBuf * kAccW <= kTmemColsB && 2 * MP <= (int)kAccW, "TMEM columns");
   // kind::f16 instruction descriptor: D f32, A fp16, B fp16, both K-major, N = 2 MP, M = 128
   static constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)((2 * MP) >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
   static_assert(kSmemAlloc <= 232448, "shared memory");
@@ -182,9 +194,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   uint64_t* afull = sempty + kSIStages;
   // cfull[a]: the MMAs of the super-block in buffer pair a are done, so its
   // accumulator is ready for the epilogue and its A buffer free for the dequant
-  uint64_t* cfull = afull + 2;
-  uint64_t* cempty = cfull + 2;
-  uint64_t* drain = cempty + 2;
+  uint64_t* cfull = afull + C::kNBuf;
+  uint64_t* cempty = cfull + C::kNBuf;
+  uint64_t* drain = cempty + C::kNBuf;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
@@ -197,7 +209,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) {
       mbar_init(&wfull[s], 1);
-      mbar_init(&wempty[s], 8);
+      mbar_init(&wempty[s], kDqWarps);
     }
     for (int s = 0; s < C::kBStages; ++s) {
       mbar_init(&bfull[s], 1);
@@ -205,12 +217,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     }
     for (int s = 0; s < kSIStages; ++s) {
       mbar_init(&sfull[s], 1);
-      mbar_init(&sempty[s], 8);
+      mbar_init(&sempty[s], kDqWarps);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&afull[a], 8);
+    for (int a = 0; a < C::kNBuf; ++a) {
+      mbar_init(&afull[a], kDqWarps);
       mbar_init(&cfull[a], 1);
-      mbar_init(&cempty[a], 8);
+      mbar_init(&cempty[a], kDqWarps);
     }
     mbar_init(drain, 1);
     *abort = 0;
@@ -221,7 +233,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     prefetch_tensormap(&wmap);
     prefetch_tensormap(&xmap);
   }
-  if (warp == 10) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemColsB)
                  : "memory");
@@ -298,18 +310,18 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           if (globaltimer_ns() - t0 > 200000000ull) break;
       }
     }
-  } else if (warp == 10) {
+  } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer
     if (lane == 0) {
       for (int i = 0; i < nloc && !*abort; ++i) {
-        const int a = i & 1;
-        if (!mbar_wait_bounded(&afull[a], (i >> 1) & 1, abort, tmo) ||
-            (i >= 2 && !mbar_wait_bounded(&cempty[a], ((i >> 1) - 1) & 1, abort, tmo))) {
+        const int a = i % C::kNBuf, use = i / C::kNBuf;
+        if (!mbar_wait_bounded(&afull[a], use & 1, abort, tmo) ||
+            (use >= 1 && !mbar_wait_bounded(&cempty[a], (use - 1) & 1, abort, tmo))) {
           if (!*abort) fail();
           break;
         }
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem + kAccCol + 128u * (uint32_t)a;
+        const uint32_t d_tmem = tmem + C::kAccCol + C::kAccW * (uint32_t)a;
         const uint32_t a_tmem = tmem + 128u * (uint32_t)a;
         const int slot = i % C::kBStages;
         const bool ok = mbar_wait_bounded(&bfull[slot], (i / C::kBStages) & 1, abort, tmo);
@@ -339,24 +351,24 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     }
   } else {
     // ---------------- dequant into TMEM + epilogue
-    const int mw = warp - 2;        // 0..7
+    const int mw = warp - 2;        // 0 .. kDqWarps - 1
     const int q = warp & 3;         // TMEM lanes 32q .. 32q+31 (fixed by the warp's rank)
-    const int hh = mw >> 2;         // K half (dequant) and input-row half (epilogue)
+    const int kp = mw >> 2;         // K part (dequant) and input-row part (epilogue) of this warp
     const int r = 32 * q + lane;    // row within the tile
     const int64_t n = (int64_t)tile * kBM + r;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    float y[C::kMh];
+    float y[C::kMq];
 #pragma unroll
-    for (int mm = 0; mm < C::kMh; ++mm) y[mm] = 0.0f;
+    for (int mm = 0; mm < C::kMq; ++mm) y[mm] = 0.0f;
 
     auto epilogue = [&](int j, uint4 hd) -> bool {
-      const int a = j & 1;
-      if (!mbar_wait_bounded(&cfull[a], (j >> 1) & 1, abort, tmo)) return false;
+      const int a = j % C::kNBuf;
+      if (!mbar_wait_bounded(&cfull[a], (j / C::kNBuf) & 1, abort, tmo)) return false;
       tc_fence_after_sync();
-      uint32_t rh[C::kMh], rl[C::kMh];
-      const uint32_t acc = tmem + lane_base + kAccCol + 128u * (uint32_t)a;
-      tmem_ld_cols<C::kMh>(acc + (uint32_t)(hh * C::kMh), rh);
-      tmem_ld_cols<C::kMh>(acc + (uint32_t)(MP + hh * C::kMh), rl);
+      uint32_t rh[C::kMq], rl[C::kMq];
+      const uint32_t acc = tmem + lane_base + C::kAccCol + C::kAccW * (uint32_t)a;
+      tmem_ld_cols<C::kMq>(acc + (uint32_t)(kp * C::kMq), rh);
+      tmem_ld_cols<C::kMq>(acc + (uint32_t)(MP + kp * C::kMq), rl);
       tmem_wait_ld();
       tc_fence_before_sync();
       __syncwarp();
@@ -375,8 +387,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         mj[4 + t] = (float)((m_hi >> (8 * t)) & 0xFF);
       }
 #pragma unroll
-      for (int mm = 0; mm < C::kMh; ++mm) {
-        const int m = hh * C::kMh + mm;
+      for (int mm = 0; mm < C::kMq; ++mm) {
+        const int m = kp * C::kMq + mm;
         const float4 s0 = S4[2 * m], s1 = S4[2 * m + 1];
         float ms = mj[0] * s0.x;
         ms = fmaf(mj[1], s0.y, ms);
@@ -395,7 +407,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       return true;
     };
 
-    uint4 hprev = make_uint4(0, 0, 0, 0);
+    // headers of the last kLag super-blocks (hq[k]: super-block i - 1 - k), for their epilogues
+    uint4 hq[C::kLag];
+#pragma unroll
+    for (int k = 0; k < C::kLag; ++k) hq[k] = make_uint4(0, 0, 0, 0);
     bool ok = true;
     for (int i = 0; i < nloc && ok; ++i) {
       const int ws = i % kWStages;
@@ -405,52 +420,65 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
       const uint8_t* rowp = smem + C::kOffW + ws * kWTileBytes + r * 144;
       const uint4 hdr = *reinterpret_cast<const uint4*>(rowp);
-      uint4 qv[4];
+      constexpr int kG = 4 / kKParts;  // 64-weight groups per warp: group g = sub-blocks 2g, 2g + 1
+      uint4 qv[2 * kG];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) qv[c] = *reinterpret_cast<const uint4*>(rowp + 16 + 64 * hh + 16 * c);
+      for (int c = 0; c < 2 * kG; ++c) qv[c] = *reinterpret_cast<const uint4*>(rowp + 16 + 32 * kG * kp + 16 * c);
       __syncwarp();
       if (lane == 0) mbar_arrive(&wempty[ws]);
 
-      // scales of this thread's four sub-blocks 4hh .. 4hh+3
-      const uint32_t scw = hh ? ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u)) : (hdr.y & 0x3F3F3F3Fu);
-      if (i >= 2 && !mbar_wait_bounded(&cfull[i & 1], ((i >> 1) - 1) & 1, abort, tmo)) {
+      const int a = i % C::kNBuf, use = i / C::kNBuf;
+      if (use >= 1 && !mbar_wait_bounded(&cfull[a], (use - 1) & 1, abort, tmo)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
 #pragma unroll
-      for (int gi = 0; gi < 2; ++gi) {
+      for (int gg = 0; gg < kG; ++gg) {
+        const int g = kG * kp + gg;
+        // 6-bit scales of sub-blocks 2g (low nibbles) and 2g + 1 (high nibbles): sub-blocks 0-3 in
+        // the low 6 bits of header bytes 4-7, sub-blocks 4-7 from the low nibbles of bytes 12-15 and
+        // the top 2 bits of bytes 4-7
+        const uint32_t scw = g >= 2 ? ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u)) : (hdr.y & 0x3F3F3F3Fu);
+        const int gi = g & 1;
         const float scl = (float)((scw >> (16 * gi)) & 0xFF), sch = (float)((scw >> (16 * gi + 8)) & 0xFF);
         const uint32_t mul_l = half2_splat(scl), add_l = half2_splat(-1024.0f * scl);
         const uint32_t mul_h = half2_splat(sch), add_h = half2_splat(-1024.0f * sch);
-        const uint32_t wv[8] = {qv[2 * gi].x,     qv[2 * gi].y,     qv[2 * gi].z,     qv[2 * gi].w,
-                                qv[2 * gi + 1].x, qv[2 * gi + 1].y, qv[2 * gi + 1].z, qv[2 * gi + 1].w};
+        const uint32_t wv[8] = {qv[2 * gg].x,     qv[2 * gg].y,     qv[2 * gg].z,     qv[2 * gg].w,
+                                qv[2 * gg + 1].x, qv[2 * gg + 1].y, qv[2 * gg + 1].z, qv[2 * gg + 1].w};
         uint32_t out[32];
 #pragma unroll
         for (int w = 0; w < 8; ++w)
           scq_word(wv[w], mul_l, add_l, mul_h, add_h, out[2 * w], out[2 * w + 1], out[16 + 2 * w],
                    out[16 + 2 * w + 1]);
-        tmem_st32(tmem + lane_base + 128u * (uint32_t)(i & 1) + (uint32_t)(64 * hh + 32 * gi), out);
+        tmem_st32(tmem + lane_base + 128u * (uint32_t)a + (uint32_t)(32 * g), out);
       }
       tmem_wait_st();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&afull[i & 1]);
-      if (i >= 1 && !epilogue(i - 1, hprev)) {
+      if (lane == 0) mbar_arrive(&afull[a]);
+      if (i >= C::kLag && !epilogue(i - C::kLag, hq[C::kLag - 1])) {
         ok = false;
         break;
       }
-      hprev = hdr;
+#pragma unroll
+      for (int k = C::kLag - 1; k > 0; --k) hq[k] = hq[k - 1];
+      hq[0] = hdr;
     }
-    if (ok && nloc > 0 && !epilogue(nloc - 1, hprev)) ok = false;
+    // the last kLag epilogues (hq[k] holds super-block nloc - 1 - k)
+#pragma unroll
+    for (int k = C::kLag - 1; k >= 0; --k) {
+      const int j = nloc - 1 - k;
+      if (ok && j >= 0 && !epilogue(j, hq[k])) ok = false;
+    }
     if (!ok && !*abort) fail();
 
     // ---------------- output
     if (p.splits == 1) {
       if (n < p.N) {
 #pragma unroll
-        for (int mm = 0; mm < C::kMh; ++mm) {
-          const int m = hh * C::kMh + mm;
+        for (int mm = 0; mm < C::kMq; ++mm) {
+          const int m = kp * C::kMq + mm;
           if (m < p.M) p.Y[(int64_t)m * p.N + n] = y[mm];
         }
       }
@@ -459,24 +487,24 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       float* part = p.partial + (int64_t)split * p.M * p.N;
       if (n < p.N) {
 #pragma unroll
-        for (int mm = 0; mm < C::kMh; ++mm) {
-          const int m = hh * C::kMh + mm;
+        for (int mm = 0; mm < C::kMq; ++mm) {
+          const int m = kp * C::kMq + mm;
           if (m < p.M) part[(int64_t)m * p.N + n] = y[mm];
         }
       }
       __threadfence();
-      named_bar_sync(1, 256);
+      named_bar_sync(1, 32 * kDqWarps);
       if (mw == 0 && lane == 0) {
         const unsigned prev = atomicAdd(&p.counters[tile], 1u);
         *last_flag = prev == (unsigned)(p.splits - 1) ? 1 : 0;
       }
-      named_bar_sync(1, 256);
+      named_bar_sync(1, 32 * kDqWarps);
       if (*last_flag) {
         __threadfence();
         if (n < p.N) {
 #pragma unroll 1
-          for (int mm = 0; mm < C::kMh; ++mm) {
-            const int m = hh * C::kMh + mm;
+          for (int mm = 0; mm < C::kMq; ++mm) {
+            const int m = kp * C::kMq + mm;
             if (m >= p.M) continue;
             float acc = 0.0f;
             for (int sp = 0; sp < p.splits; ++sp) acc += __ldcg(p.partial + ((int64_t)sp * p.M + m) * p.N + n);
@@ -488,7 +516,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 10) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after_sync();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemColsB) : "memory");

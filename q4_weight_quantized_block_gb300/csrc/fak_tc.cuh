@@ -88,6 +88,11 @@ template <int N>
 FAK_DEV void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]);
 
 template <>
+FAK_DEV void tmem_ld_cols<2>(uint32_t taddr, uint32_t (&r)[2]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(taddr));
+}
+
+template <>
 FAK_DEV void tmem_ld_cols<4>(uint32_t taddr, uint32_t (&r)[4]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
