@@ -34,6 +34,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -153,6 +154,7 @@ struct MixDesc {
   float* vc;             // FA: [nkv][max_ctx][256]
   int32_t nk, nv, nq, nkv, rot, max_ctx;
   float theta, eps;
+  double inv_freq[128];  // FA: theta^(-2i/rot) for i < rot / 2, in double (host pow)
 };
 
 __device__ int g_fak_status;  // status word of the stateless entry points
@@ -927,6 +929,42 @@ __device__ __forceinline__ bool poll1(const float* p, uint32_t want, float& v, c
   }
 }
 
+// Up to N tagged values at once: every load is in flight together, then only the stale ones are
+// read again until all carry their expected tag (bounded like every wait).  use[k] false: slot k
+// is skipped and v[k] left as it is.
+template <int N>
+__device__ __forceinline__ bool poll_n(const float* const (&p)[N], const uint32_t (&want)[N], const bool (&use)[N],
+                                       float (&v)[N], const EngParams& P, volatile int* abort) {
+  uint32_t stale = 0;
+#pragma unroll
+  for (int k = 0; k < N; ++k)
+    if (use[k]) v[k] = ld_relaxed_f(p[k]);
+#pragma unroll
+  for (int k = 0; k < N; ++k)
+    if (use[k] && (__float_as_uint(v[k]) & 1u) != want[k]) stale |= 1u << k;
+  uint64_t t0 = 0;
+  for (uint32_t it = 0; stale; ++it) {
+    if (*abort) return false;
+    if (it == 0) {
+      t0 = globaltimer_ns();
+    } else if (globaltimer_ns() - t0 > P.timeout_ns) {
+      set_error(P, FAK_ERR_TIMEOUT, abort);
+      return false;
+    }
+    __nanosleep(64);
+#pragma unroll
+    for (int k = 0; k < N; ++k)
+      if ((stale >> k) & 1u) v[k] = ld_relaxed_f(p[k]);
+#pragma unroll
+    for (int k = 0; k < N; ++k)
+      if (((stale >> k) & 1u) && (__float_as_uint(v[k]) & 1u) == want[k]) stale &= ~(1u << k);
+  }
+#pragma unroll
+  for (int k = 0; k < N; ++k)
+    if (use[k]) v[k] = untag(v[k]);
+  return true;
+}
+
 // Sum over the first `nw` warps' values of `v` (block-wide; every thread gets the same sum,
 // summed in warp order).  scratch: at least nw floats; the caller's threads all call it.
 __device__ __forceinline__ float block_sum(float v, int nw, float* scratch, int ctid) {
@@ -963,18 +1001,31 @@ __device__ void gdn_step(const EngParams& P, const EngOp& op, uint8_t* smem, int
   // conv channel of this thread: q (key head kh), k (key head kh), v (value head h)
   const int c = ctid < 128 ? kh * 128 + ctid
                            : (ctid < 256 ? nk * 128 + kh * 128 + (ctid - 128) : 2 * nk * 128 + h * 128 + (ctid - 256));
-  float xin = 0.0f, zv = 0.0f, bv = 0.0f, av = 0.0f;
-  bool ok = poll1(M.t + c, want, xin, P, abort);
-  if (ok && ctid < 128) ok = poll1(M.t + conv_dim + h * 128 + ctid, want, zv, P, abort);
-  if (ok && ctid == 0) ok = poll1(M.t + conv_dim + nv * 128 + h, want, bv, P, abort);
-  if (ok && ctid == 0) ok = poll1(M.t + conv_dim + nv * 128 + nv + h, want, av, P, abort);
+  // What does not depend on this token's input is requested first, so that its latency overlaps
+  // the wait for the in_proj output: the head's state (64 KB, written by the previous token and
+  // long evicted from L2) is prefetched into L2; this thread's conv channel state and taps, the
+  // gate parameters and the norm gain are loaded.
+  const int j = ctid & 127, r = ctid >> 7;
+  float* Sh = M.S + (size_t)h * 128 * 128;
+  for (int line = ctid; line < 128 * 128 * 4 / 128; line += kConsumerThreads)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(Sh + line * 32));
+  const float* so = M.conv_state + ((size_t)par * conv_dim + c) * 3;
+  const float4 w = *reinterpret_cast<const float4*>(M.conv_w + (size_t)c * 4);
+  const float s0 = so[0], s1 = so[1], s2 = so[2];
+  const float dtb = ctid == 0 ? M.dt_bias[h] : 0.0f, alog = ctid == 0 ? M.a_log[h] : 0.0f;
+  const float nwj = ctid < 128 ? M.norm_w[j] : 0.0f;
+  // the step's inputs, all in flight at once: the conv channel, z (warps 0-3), b and a (thread 0)
+  const float* const pin[4] = {M.t + c, M.t + conv_dim + h * 128 + (ctid & 127), M.t + conv_dim + nv * 128 + h,
+                               M.t + conv_dim + nv * 128 + nv + h};
+  const uint32_t wants[4] = {want, want, want, want};
+  const bool use[4] = {true, ctid < 128, ctid == 0, ctid == 0};
+  float vin[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  poll_n<4>(pin, wants, use, vin, P, abort);
+  const float xin = vin[0], zv = vin[1], bv = vin[2], av = vin[3];
   named_bar_sync(1, kConsumerThreads);
   if (*abort) return;
   {
-    const float* so = M.conv_state + ((size_t)par * conv_dim + c) * 3;
     float* sn = M.conv_state + ((size_t)(par ^ 1) * conv_dim + c) * 3;
-    const float4 w = *reinterpret_cast<const float4*>(M.conv_w + (size_t)c * 4);
-    const float s0 = so[0], s1 = so[1], s2 = so[2];
     const float acc = fmaf(w.w, xin, fmaf(w.z, s2, fmaf(w.y, s1, w.x * s0)));
     y[ctid] = silu_f(acc);
     // the q and k channels are shared by `ratio` value heads: the first one writes their new state
@@ -986,9 +1037,9 @@ __device__ void gdn_step(const EngParams& P, const EngOp& op, uint8_t* smem, int
     if (ctid < 128) zs[ctid] = silu_f(zv);
     if (ctid == 0) {
       gates[0] = 1.0f / (1.0f + expf(-bv));
-      const float sp = av + M.dt_bias[h];
+      const float sp = av + dtb;
       const float soft = sp > 20.0f ? sp : log1pf(expf(sp));
-      gates[1] = expf(-expf(M.a_log[h]) * soft);
+      gates[1] = expf(-expf(alog) * soft);
     }
   }
   named_bar_sync(1, kConsumerThreads);
@@ -1004,8 +1055,6 @@ __device__ void gdn_step(const EngParams& P, const EngOp& op, uint8_t* smem, int
   const float rq = 1.0f / sqrtf(qq + M.eps) / sqrtf(128.0f), rk = 1.0f / sqrtf(kk + M.eps);
   const float beta = gates[0], alpha = gates[1];
   // state update: column j, rows [43 r, 43 r + 43)
-  const int j = ctid & 127, r = ctid >> 7;
-  float* Sh = M.S + (size_t)h * 128 * 128;
   float sreg[43];
   float kv = 0.0f;
 #pragma unroll
@@ -1038,9 +1087,13 @@ __device__ void gdn_step(const EngParams& P, const EngOp& op, uint8_t* smem, int
   const float ss = block_sum(ctid < 128 ? oj * oj : 0.0f, 4, scr + 8, ctid);
   if (ctid < 128) {
     const float rn = 1.0f / sqrtf(ss / 128.0f + M.eps);
-    st_tagged(M.out + h * 128 + j, oj * rn * M.norm_w[j] * zs[j], otag);
+    st_tagged(M.out + h * 128 + j, oj * rn * nwj * zs[j], otag);
   }
 }
+
+// q, k, v, gate (4 x 256), reduction scratch (32) and the scores (max_ctx <= 8192) fit in the x-limb
+// region the step reuses
+static_assert((4 * 256 + 32 + 8192) * 4 <= kMaxSuper * kSuperBytes, "attention scratch exceeds the x-limb region");
 
 // Gated attention step of query head h = blockIdx.x at position *P.pos: qk-norm, RoPE, the
 // KV-cache append (by the first query head of each KV group), softmax over positions 0..pos
@@ -1065,14 +1118,15 @@ __device__ void attn_step(const EngParams& P, const EngOp& op, uint8_t* smem, in
   float* scr = gs + 256;                               // [32]
   float* sc = scr + 32;                                // [max_ctx] scores, then weights
   const int d = ctid;
-  float qv = 0.0f, gv = 0.0f, kv = 0.0f, vv = 0.0f;
-  bool ok = true;
-  if (d < 256) {
-    ok = poll1(M.t + h * 512 + d, want, qv, P, abort);
-    if (ok) ok = poll1(M.t + h * 512 + 256 + d, want, gv, P, abort);
-    if (ok) ok = poll1(M.kin + g * 256 + d, want_kv, kv, P, abort);
-    if (ok) ok = poll1(M.vin + g * 256 + d, want_kv, vv, P, abort);
-  }
+  // q, gate, k and v of this position, all in flight at once
+  const int dd = d & 255;
+  const float* const pin[4] = {M.t + h * 512 + dd, M.t + h * 512 + 256 + dd, M.kin + g * 256 + dd,
+                               M.vin + g * 256 + dd};
+  const uint32_t wants[4] = {want, want, want_kv, want_kv};
+  const bool use[4] = {d < 256, d < 256, d < 256, d < 256};
+  float vin[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  poll_n<4>(pin, wants, use, vin, P, abort);
+  const float qv = vin[0], gv = vin[1], kv = vin[2], vv = vin[3];
   named_bar_sync(1, kConsumerThreads);
   if (*abort) return;
   const float sq = block_sum(d < 256 ? qv * qv : 0.0f, 8, scr, ctid);
@@ -1086,10 +1140,12 @@ __device__ void attn_step(const EngParams& P, const EngOp& op, uint8_t* smem, in
   named_bar_sync(1, kConsumerThreads);
   const int half = M.rot / 2;
   if (d < half) {
-    // the angle in double precision: pos * theta^(-2d/rot) reaches thousands of radians
-    double sn, cs;
-    sincos((double)pos * pow((double)M.theta, -2.0 * (double)d / (double)M.rot), &sn, &cs);
-    const float c = (float)cs, s = (float)sn;
+    // the angle pos * theta^(-2d/rot) in double precision (it reaches thousands of radians),
+    // reduced modulo 2 pi in double; sine and cosine of the reduced angle in single precision
+    const double ang = (double)pos * M.inv_freq[d];
+    const double red = ang - 6.283185307179586 * rint(ang * 0.15915494309189535);
+    float s, c;
+    sincosf((float)red, &s, &c);
     const float q1 = qs[d], q2 = qs[d + half], k1 = ks[d], k2 = ks[d + half];
     qs[d] = q1 * c - q2 * s;
     qs[d + half] = q2 * c + q1 * s;
@@ -1103,16 +1159,28 @@ __device__ void attn_step(const EngParams& P, const EngOp& op, uint8_t* smem, in
     kcp[(size_t)pos * 256 + d] = ks[d];
     vcp[(size_t)pos * 256 + d] = vs[d];
   }
-  // scores: warp w takes positions w, w + 12, ...; lane l dims 8l..8l+7
+  // scores: warp w takes positions w, w + 12, ... (two at a time, their key rows loaded as two
+  // float4 per lane); lane l dims 8l..8l+7; the current position's key comes from shared memory
   const int w = ctid >> 5, lane = ctid & 31;
-  for (int sidx = w; sidx <= pos; sidx += kNumConsumerWarps) {
-    const float* kr = sidx == pos ? ks : kcp + (size_t)sidx * 256;
+#pragma unroll 2
+  for (int sidx = w; sidx < pos; sidx += kNumConsumerWarps) {
+    const float4* kr = reinterpret_cast<const float4*>(kcp + (size_t)sidx * 256 + lane * 8);
+    const float4 k0 = __ldcg(kr), k1 = __ldcg(kr + 1);
+    const float kk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
     float acc = 0.0f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc = fmaf(qs[lane * 8 + e], kr[lane * 8 + e], acc);
+    for (int e = 0; e < 8; ++e) acc = fmaf(qs[lane * 8 + e], kk[e], acc);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) sc[sidx] = acc * 0.0625f;  // 1 / sqrt(256)
+  }
+  if (w == pos % kNumConsumerWarps) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc = fmaf(qs[lane * 8 + e], ks[lane * 8 + e], acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) sc[pos] = acc * 0.0625f;
   }
   named_bar_sync(1, kConsumerThreads);
   float mx = -INFINITY;
@@ -1132,8 +1200,11 @@ __device__ void attn_step(const EngParams& P, const EngOp& op, uint8_t* smem, in
   }
   const float sum = block_sum(se, kNumConsumerWarps, scr, ctid);
   if (d < 256) {
+    // the cached positions in order, sixteen loads in flight, then this position's own value
     float acc = 0.0f;
-    for (int sidx = 0; sidx <= pos; ++sidx) acc = fmaf(sc[sidx], sidx == pos ? vs[d] : vcp[(size_t)sidx * 256 + d], acc);
+#pragma unroll 16
+    for (int sidx = 0; sidx < pos; ++sidx) acc = fmaf(sc[sidx], __ldcg(vcp + (size_t)sidx * 256 + d), acc);
+    acc = fmaf(sc[pos], vs[d], acc);
     st_tagged(M.out + h * 256 + d, acc / sum * gs[d], otag);
   }
 }
@@ -1917,6 +1988,8 @@ extern "C" int fak_decode_create(const fak_decode_desc* d, fak_decode** out) {
       md.rot = m.fa_rot;
       md.max_ctx = m.max_ctx;
       md.theta = m.rope_theta;
+      for (int i = 0; i < m.fa_rot / 2; ++i)
+        md.inv_freq[i] = std::pow((double)m.rope_theta, -2.0 * (double)i / (double)m.fa_rot);
       md.eps = m.eps;
       if (d->layers[l].kind == FAK_LAYER_GDN) {
         md.conv_w = M.conv_w;
