@@ -402,7 +402,8 @@ void fak_decode_destroy(fak_decode* ctx);
  * an interleaved copy of every layer's gate / up weights (2 * d_ff * d_model /
  * 256 * 144 bytes per layer, for the SwiGLU fused into the GEMM epilogue), and
  * records the forward into a CUDA graph.  The weights stay caller-owned and
- * must outlive the context.  d_model <= 8192.
+ * must outlive the context.  d_model <= 8192; gdn_in and fa_qg multiples of 4,
+ * n_mix of 256, d_ff of 64 (else FAK_ERR_SHAPE).
  * fak_prefill_run: d_tokens (device int32 [P]) in; d_tok_out (device int32) =
  * the argmax of the last token's logits; d_logits (device f32 [vocab], nullable).
  * One graph launch (plus the copies of the tokens in and the results out),

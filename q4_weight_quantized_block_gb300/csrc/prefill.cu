@@ -117,10 +117,30 @@ __global__ void __launch_bounds__(kRowThreads) last_rms_kernel(const float* hrow
 }
 
 // X2[p, i] = bf16(T[p, i]) for i < n (the out_proj / o input: the first n channels of t).
+// ld % 4 == 0, n % 4 == 0: four channels per float4 load and one 8-byte store, eight loads of a
+// thread in flight before its stores.
 __global__ void __launch_bounds__(kRowThreads) slice_bf16_kernel(const float* T, int64_t ld, int n,
                                                                  __nv_bfloat16* X2) {
   const int64_t p = blockIdx.x;
-  for (int i = threadIdx.x; i < n; i += kRowThreads) X2[p * n + i] = __float2bfloat16_rn(T[p * ld + i]);
+  const float4* src = reinterpret_cast<const float4*>(T + p * ld);
+  uint2* dst = reinterpret_cast<uint2*>(X2 + p * n);
+  const int n4 = n / 4;
+  for (int i0 = threadIdx.x; i0 < n4; i0 += 8 * kRowThreads) {
+    float4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = i0 + k * kRowThreads;
+      if (i < n4) v[k] = src[i];
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = i0 + k * kRowThreads;
+      if (i < n4) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v[k].x, v[k].y), b = __floats2bfloat162_rn(v[k].z, v[k].w);
+        dst[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+      }
+    }
+  }
 }
 
 // argmax with the lowest index on ties (NaN skipped): every thread folds its values into one
@@ -247,7 +267,7 @@ extern "C" int fak_prefill_create(const fak_decode_desc* d, int64_t P, fak_prefi
   auto okdim = [](int64_t v) { return v >= 256 && v % 256 == 0 && v <= FAK_ENGINE_MAX_K; };
   if (P < 1 || P > 16384 || d->n_layers < 0 || !okdim(d->d_model) || d->d_model > 8192 || !okdim(d->d_ff) ||
       !okdim(d->n_mix) || d->vocab < 1 || d->gdn_in < 1 || d->fa_qg < 1 ||
-      d->fa_kv < 1 || d->d_ff % 64 || d->n_mix % 256)
+      d->fa_kv < 1 || d->d_ff % 64 || d->n_mix % 256 || d->gdn_in % 4 || d->fa_qg % 4)
     return FAK_ERR_SHAPE;
   for (int l = 0; l < d->n_layers; ++l) {
     const fak_layer_desc& L = d->layers[l];

@@ -102,3 +102,26 @@ def test_q8_0_packer_bit_exact_with_oracle(fak):
     for w in [_edge_tensor(), synth.normal(3, 900000, (2048, 5120), 0.02)]:
         a, b = fak.fak_q8_0_pack(w), oracle.q8_0_pack(w)
         assert np.array_equal(a, b)
+
+
+def test_prefill_create_rejects_bad_shapes_before_any_device_call(fak):
+    ok_ptr = 1 << 20
+    layer = {"kind": fak.FAK_LAYER_GDN, "w_in": ok_ptr, "w_out": ok_ptr, "w_gate": ok_ptr, "w_up": ok_ptr,
+             "w_down": ok_ptr}
+    good = dict(d_model=256, d_ff=512, vocab=300, gdn_in=640, fa_qg=512, fa_kv=256, n_mix=256)
+    bad = [dict(gdn_in=642),     # in_proj rows not a multiple of 4 (the bf16 slice reads float4)
+           dict(fa_qg=514),      # q+gate rows not a multiple of 4
+           dict(n_mix=300),      # out_proj input not whole super-blocks
+           dict(d_ff=544),       # d_ff not a multiple of 64 (gate/up interleave)
+           dict(d_model=200),    # K not whole super-blocks
+           dict(d_model=8448)]   # d_model above the RMSNorm kernel's 8192
+    for change in bad:
+        args = dict(good, **change)
+        with pytest.raises(fak.FakError) as ei:
+            fak.PrefillContext(args["d_model"], args["d_ff"], args["vocab"], args["gdn_in"], args["fa_qg"],
+                               args["fa_kv"], args["n_mix"], [layer], ok_ptr, ok_ptr, 64)
+        assert ei.value.status == 2, change
+    for n_tokens in (0, 16385):
+        with pytest.raises(fak.FakError) as ei:
+            fak.PrefillContext(256, 512, 300, 640, 512, 256, 256, [layer], ok_ptr, ok_ptr, n_tokens)
+        assert ei.value.status == 2

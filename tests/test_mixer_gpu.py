@@ -89,6 +89,29 @@ def test_mixer_decode_eight_layers_two_periods(fak):
     dec.close()
 
 
+def test_mixer_decode_long_context(fak):
+    # 1100 positions: rotary angles up to 1100 rad (reduced modulo 2 pi on the GPU), key and value
+    # passes over more than a thousand cached rows (many full unrolled batches and a remainder)
+    m, d, layers, params, lm, emb = small_mixer_model(seed=17, **SMALL)
+    ctx = gpu_context(fak, m, d, layers, params, lm, emb, max_ctx=1200, **SMALL)
+    dec = oracle.MixerDecoder(m, d, params, max_ctx=1200)
+    tin = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tout = torch.zeros(1, dtype=torch.int32, device="cuda")
+    logits = torch.empty(SMALL["V"], device="cuda")
+    tok = 7
+    for step in range(1100):
+        tin.fill_(tok)
+        ctx.step(tin, tout, logits)
+        rt, rl, ra, _ = dec.decode_token(tok)
+        if step % 50 == 0 or step >= 1090:
+            assert ctx.status() == 0
+            check_f32(logits.cpu().numpy(), rl, ra, "long context, position %d" % step)
+        tok = rt
+    assert ctx.status() == 0
+    ctx.close()
+    dec.close()
+
+
 def test_mixer_one_launch_equals_per_matmul_and_reset(fak):
     m, d, layers, params, lm, emb = small_mixer_model(seed=14, **SMALL)
     one = gpu_context(fak, m, d, layers, params, lm, emb, mode=0, **SMALL)
