@@ -311,7 +311,10 @@ typedef struct {
  * Supported: dk = dv = 128, dh = 256, conv = 4, nv <= 152 and nq <= 152 (one
  * CTA per head), nv % nk == 0, nq % nkv == 0, rot even and <= dh,
  * n_mix == nv*dv == nq*dh.  A step past max_ctx positions records
- * FAK_ERR_DEVICE (attention uses the first max_ctx positions only).
+ * FAK_ERR_DEVICE (attention uses the first max_ctx positions only): its
+ * attention output is zero, the KV cache is not written, the step still ends
+ * at once, and fak_decode_status, on reporting it, clears the state (the next
+ * step is position 0 of a new sequence).
  */
 typedef struct {
     const float* conv_w;     /* GDN: [2*nk*dk + nv*dv][4] f32, device */

@@ -1104,13 +1104,16 @@ __device__ void attn_step(const EngParams& P, const EngOp& op, uint8_t* smem, in
   if (h >= M.nq) return;
   const int grp = M.nq / M.nkv, g = h / grp;
   const int pos = *P.pos;
-  if (pos < 0 || pos >= M.max_ctx) {
-    if (ctid == 0) atomicCAS(P.err ? P.err : &g_fak_status, 0, FAK_ERR_DEVICE);
-    return;
-  }
   const uint32_t want = tag_in_par(op.tags) ^ ((P.flip >> tag_in_buf(op.tags)) & 1u);
   const uint32_t want_kv = 1u ^ ((P.flip >> 3) & 1u);  // every k / v slice: version 1 of its token
   const uint32_t otag = tag_out_par(op.tags, 0) ^ ((P.flip >> tag_out_buf(op.tags, 0)) & 1u);
+  if (pos < 0 || pos >= M.max_ctx) {
+    // past the cache: record the error, and still hand the next step a (zero) output so that the
+    // token ends at once instead of in the readers' timeout; nothing is written to the cache
+    if (ctid == 0) atomicCAS(P.err ? P.err : &g_fak_status, 0, FAK_ERR_DEVICE);
+    if (ctid < 256) st_tagged(M.out + h * 256 + ctid, 0.0f, otag);
+    return;
+  }
   float* qs = reinterpret_cast<float*>(smem + kOffX);  // [256] normed, rotated q
   float* ks = qs + 256;                                // [256] normed, rotated k of this position
   float* vs = ks + 256;                                // [256]

@@ -153,6 +153,33 @@ def test_mixer_decode_full_width_matches_oracle(fak):
     dec.close()
 
 
+def test_mixer_step_past_max_ctx_reports_and_recovers(fak):
+    # max_ctx = 4: the fifth position has no cache row.  The step records FAK_ERR_DEVICE without
+    # waiting out the readers' timeout, reading the status clears the state, and the next step is
+    # position 0 of a new sequence again (bit for bit the first step's logits).
+    import time
+    m, d, layers, params, lm, emb = small_mixer_model(seed=18, **SMALL)
+    ctx = gpu_context(fak, m, d, layers, params, lm, emb, max_ctx=4, **SMALL)
+    tin = torch.full((1,), 3, dtype=torch.int32, device="cuda")
+    tout = torch.zeros(1, dtype=torch.int32, device="cuda")
+    logits = torch.empty(SMALL["V"], device="cuda")
+    first = None
+    for step in range(4):
+        ctx.step(tin, tout, logits)
+        assert ctx.status() == 0
+        if first is None:
+            first = logits.cpu().numpy().copy()
+    t0 = time.time()
+    ctx.step(tin, tout, logits)
+    st = ctx.status()
+    assert st == 7, st  # FAK_ERR_DEVICE
+    assert time.time() - t0 < 0.5
+    ctx.step(tin, tout, logits)
+    assert ctx.status() == 0
+    assert np.array_equal(logits.cpu().numpy().view(np.uint32), first.view(np.uint32))
+    ctx.close()
+
+
 def test_mixer_rejects_bad_shapes(fak):
     m, d, layers, params, lm, emb = small_mixer_model(seed=16, **SMALL)
     with pytest.raises(fak.FakError) as ei:

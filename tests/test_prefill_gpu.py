@@ -91,6 +91,11 @@ def test_prefill_small_stack(fak):
     run_case(fak, 70, 4, 300, D=256, F=512, V=1000, GI=640, QG=512, KV=256, NM=256)
 
 
+def test_prefill_single_token(fak):
+    # P = 1: every GEMM has one token in its only token tile
+    run_case(fak, 73, 4, 1, D=256, F=512, V=1000, GI=640, QG=512, KV=256, NM=256)
+
+
 def test_prefill_gdn_in_not_a_multiple_of_128(fak):
     # the 27B GDN in_proj has 16480 rows: its last GEMM row tile is partial
     run_case(fak, 71, 4, 64, D=512, F=1024, V=512, GI=16480, QG=1024, KV=256, NM=512)
