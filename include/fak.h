@@ -403,10 +403,12 @@ void fak_decode_destroy(fak_decode* ctx);
  *
  * fak_prefill_create allocates the activations for P tokens (1 <= P <= 16384),
  * an interleaved copy of every layer's gate / up weights (2 * d_ff * d_model /
- * 256 * 144 bytes per layer, for the SwiGLU fused into the GEMM epilogue), and
+ * 256 * 144 bytes per layer, for the SwiGLU fused into the GEMM epilogue), a
+ * copy of every FA layer's q+gate, k and v weights as one matrix ((fa_qg + 2 *
+ * fa_kv) * d_model / 256 * 144 bytes, so that the three share one GEMM), and
  * records the forward into a CUDA graph.  The weights stay caller-owned and
  * must outlive the context.  d_model <= 8192; gdn_in and fa_qg multiples of 4,
- * n_mix of 256, d_ff of 64 (else FAK_ERR_SHAPE).
+ * fa_kv of 2, n_mix of 256, d_ff of 64 (else FAK_ERR_SHAPE).
  * fak_prefill_run: d_tokens (device int32 [P]) in; d_tok_out (device int32) =
  * the argmax of the last token's logits; d_logits (device f32 [vocab], nullable).
  * One graph launch (plus the copies of the tokens in and the results out),

@@ -177,8 +177,7 @@ struct fak_prefill {
   int32_t* toks = nullptr;
   float* h = nullptr;              // [P, D]
   __nv_bfloat16* n = nullptr;      // [P, D]
-  float* T = nullptr;              // [P, max(gdn_in, fa_qg)]
-  float* KV = nullptr;             // [P, fa_kv] (FA k / v projections, not read further)
+  float* T = nullptr;              // [P, max(gdn_in, fa_qg + 2 fa_kv)]
   __nv_bfloat16* X2 = nullptr;     // [P, max(n_mix, d_ff)]
   float* Y = nullptr;              // [P, D]
   float* nlast = nullptr;          // [D]
@@ -186,6 +185,7 @@ struct fak_prefill {
   unsigned long long* slot = nullptr;
   int32_t* tok = nullptr;
   std::vector<uint8_t*> w13;       // per layer: gate / up rows interleaved for the fused SwiGLU GEMM
+  std::vector<uint8_t*> wqkv;      // per FA layer: q+gate, k and v rows in one matrix (one GEMM); GDN: null
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
   size_t kernels = 0;
@@ -198,11 +198,11 @@ void free_prefill(fak_prefill* c) {
   if (c->exec) cudaGraphExecDestroy(c->exec);
   if (c->graph) cudaGraphDestroy(c->graph);
   for (uint8_t* w : c->w13) cudaFree(w);
+  for (uint8_t* w : c->wqkv) cudaFree(w);
   cudaFree(c->toks);
   cudaFree(c->h);
   cudaFree(c->n);
   cudaFree(c->T);
-  cudaFree(c->KV);
   cudaFree(c->X2);
   cudaFree(c->Y);
   cudaFree(c->nlast);
@@ -225,15 +225,14 @@ int record_forward(fak_prefill* c, cudaStream_t s) {
   const float* pending = nullptr;  // a matmul output still to be added into h
   for (int l = 0; l < d.n_layers; ++l) {
     const fak_layer_desc& L = c->layers[l];
-    const int64_t nin = L.kind == FAK_LAYER_GDN ? d.gdn_in : d.fa_qg;
+    // FA: q+gate, k and v share their input, so they run as one GEMM on the concatenated copy
+    // (t[:, fa_qg:] holds k and v: they belong to the forward's work; the mixer body that reads them
+    // is left out)
+    const bool fa = L.kind == FAK_LAYER_FA;
+    const int64_t nin = fa ? d.fa_qg + 2 * d.fa_kv : d.gdn_in;
     add_rms_bf16_kernel<<<(unsigned)P, kRowThreads, 0, s>>>(c->h, pending, D, d.eps, c->n);
     if ((st = launch_status(cudaSuccess)) != FAK_OK) return st;
-    if ((st = fak_q4k_gemm(L.w_in, nin, D, c->n, P, c->T, s)) != FAK_OK) return st;
-    if (L.kind == FAK_LAYER_FA) {
-      // the k and v projections belong to the forward's work; the mixer body that reads them is left out
-      if ((st = fak_q4k_gemm(L.w_k, d.fa_kv, D, c->n, P, c->KV, s)) != FAK_OK) return st;
-      if ((st = fak_q4k_gemm(L.w_v, d.fa_kv, D, c->n, P, c->KV, s)) != FAK_OK) return st;
-    }
+    if ((st = fak_q4k_gemm(fa ? c->wqkv[l] : L.w_in, nin, D, c->n, P, c->T, s)) != FAK_OK) return st;
     slice_bf16_kernel<<<(unsigned)P, kRowThreads, 0, s>>>(c->T, nin, d.n_mix, c->X2);
     if ((st = launch_status(cudaSuccess)) != FAK_OK) return st;
     if ((st = fak_q4k_gemm(L.w_out, D, d.n_mix, c->X2, P, c->Y, s)) != FAK_OK) return st;
@@ -267,7 +266,7 @@ extern "C" int fak_prefill_create(const fak_decode_desc* d, int64_t P, fak_prefi
   auto okdim = [](int64_t v) { return v >= 256 && v % 256 == 0 && v <= FAK_ENGINE_MAX_K; };
   if (P < 1 || P > 16384 || d->n_layers < 0 || !okdim(d->d_model) || d->d_model > 8192 || !okdim(d->d_ff) ||
       !okdim(d->n_mix) || d->vocab < 1 || d->gdn_in < 1 || d->fa_qg < 1 ||
-      d->fa_kv < 1 || d->d_ff % 64 || d->n_mix % 256 || d->gdn_in % 4 || d->fa_qg % 4)
+      d->fa_kv < 1 || d->d_ff % 64 || d->n_mix % 256 || d->gdn_in % 4 || d->fa_qg % 4 || d->fa_kv % 2)
     return FAK_ERR_SHAPE;
   for (int l = 0; l < d->n_layers; ++l) {
     const fak_layer_desc& L = d->layers[l];
@@ -284,19 +283,24 @@ extern "C" int fak_prefill_create(const fak_decode_desc* d, int64_t P, fak_prefi
   c->layers.assign(d->layers, d->layers + d->n_layers);
   c->desc.layers = c->layers.data();
   c->P = P;
-  const int64_t D = d->d_model, F = d->d_ff, tn = std::max(d->gdn_in, d->fa_qg);
+  const int64_t D = d->d_model, F = d->d_ff, tn = std::max(d->gdn_in, d->fa_qg + 2 * d->fa_kv);
   const int64_t x2 = std::max<int64_t>(d->n_mix, F);
   bool ok = cudaMalloc(&c->toks, P * 4) == cudaSuccess && cudaMalloc(&c->h, P * D * 4) == cudaSuccess &&
             cudaMalloc(&c->n, P * D * 2) == cudaSuccess && cudaMalloc(&c->T, P * tn * 4) == cudaSuccess &&
-            cudaMalloc(&c->KV, P * d->fa_kv * 4) == cudaSuccess && cudaMalloc(&c->X2, P * x2 * 2) == cudaSuccess &&
+            cudaMalloc(&c->X2, P * x2 * 2) == cudaSuccess &&
             cudaMalloc(&c->Y, P * D * 4) == cudaSuccess && cudaMalloc(&c->nlast, D * 4) == cudaSuccess &&
             cudaMalloc(&c->logits, (size_t)d->vocab * 4) == cudaSuccess &&
             cudaMalloc(&c->slot, sizeof(unsigned long long)) == cudaSuccess && cudaMalloc(&c->tok, 4) == cudaSuccess;
   const size_t w13_bytes = (size_t)(2 * F) * (D / 256) * 144;
+  const size_t row_bytes = (size_t)(D / 256) * 144;
   for (int l = 0; ok && l < d->n_layers; ++l) {
     uint8_t* w = nullptr;
     ok = cudaMalloc(&w, w13_bytes) == cudaSuccess;
     if (ok) c->w13.push_back(w);
+    uint8_t* q = nullptr;
+    if (ok && d->layers[l].kind == FAK_LAYER_FA)
+      ok = cudaMalloc(&q, (size_t)(d->fa_qg + 2 * d->fa_kv) * row_bytes) == cudaSuccess;
+    if (ok) c->wqkv.push_back(q);
   }
   if (!ok) {
     (void)cudaGetLastError();
@@ -309,8 +313,19 @@ extern "C" int fak_prefill_create(const fak_decode_desc* d, int64_t P, fak_prefi
     return FAK_ERR_CUDA;
   }
   int st = FAK_OK;
-  for (int l = 0; st == FAK_OK && l < d->n_layers; ++l)
+  for (int l = 0; st == FAK_OK && l < d->n_layers; ++l) {
     st = fak_q4k_interleave_gate_up(c->layers[l].w_gate, c->layers[l].w_up, F, D, c->w13[l], s);
+    if (st == FAK_OK && c->wqkv[l]) {
+      // rows are contiguous Q4_K blocks: the concatenation is three plain copies
+      const fak_layer_desc& L = c->layers[l];
+      uint8_t* q = c->wqkv[l];
+      const size_t bq = (size_t)d->fa_qg * row_bytes, bk = (size_t)d->fa_kv * row_bytes;
+      cudaError_t e = cudaMemcpyAsync(q, L.w_in, bq, cudaMemcpyDeviceToDevice, s);
+      if (e == cudaSuccess) e = cudaMemcpyAsync(q + bq, L.w_k, bk, cudaMemcpyDeviceToDevice, s);
+      if (e == cudaSuccess) e = cudaMemcpyAsync(q + bq + bk, L.w_v, bk, cudaMemcpyDeviceToDevice, s);
+      st = fak_cuda_status(e);
+    }
+  }
   if (st == FAK_OK) st = fak_cuda_status(cudaStreamSynchronize(s));
   // the forward recorded once into a graph: each prefill is then one submission
   if (st == FAK_OK) st = fak_cuda_status(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));

@@ -111,6 +111,7 @@ def test_prefill_create_rejects_bad_shapes_before_any_device_call(fak):
     good = dict(d_model=256, d_ff=512, vocab=300, gdn_in=640, fa_qg=512, fa_kv=256, n_mix=256)
     bad = [dict(gdn_in=642),     # in_proj rows not a multiple of 4 (the bf16 slice reads float4)
            dict(fa_qg=514),      # q+gate rows not a multiple of 4
+           dict(fa_kv=255),      # q+gate, k, v concatenated: the row width must stay a multiple of 4
            dict(n_mix=300),      # out_proj input not whole super-blocks
            dict(d_ff=544),       # d_ff not a multiple of 64 (gate/up interleave)
            dict(d_model=200),    # K not whole super-blocks
