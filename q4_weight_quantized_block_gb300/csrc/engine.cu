@@ -1225,6 +1225,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
   float* bestv = red + 16;                                          // [16]
   int* besti = reinterpret_cast<int*>(red + 32);                    // [16]
   volatile int* abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 192);
+  int* wend = reinterpret_cast<int*>(smem + kOffMisc + 200);        // [12] each warp's last unit (split mode)
   if (ctid == 0) *abort = 0;
   uint8_t* mybuf = smem + kOffRing + (kBuffers * cw) * kStageBytes;
   const unsigned G = gridDim.x;
@@ -1414,7 +1415,9 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       ahead_due = !ahead && ic_ok && pl.u1 > pl.u0;
       if (pl.split) {
         // sum each row's segments in slab order (the ends of warp runs inside its group, then the
-        // group end), one thread per (group, output row slot), and write the row
+        // group end), one thread per (group, output row slot), and write the row; each warp
+        // publishes where its run ends, so the combining threads need no divisions
+        if (lane == 0) wend[cw] = pl.u1 - 1;
         named_bar_sync(1, kConsumerThreads);
         for (int t = ctid; t < pl.ngroups * kSlots; t += kConsumerThreads) {
           const int gi = t / kSlots, r = t % kSlots;
@@ -1426,7 +1429,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           float v = 0.0f, vu = 0.0f;
           int last = -1;
           for (int w = 0; w < kNumConsumerWarps - 1; ++w) {
-            const int bw = pl.total * (w + 1) / kNumConsumerWarps - 1;
+            const int bw = wend[w];
             if (bw >= b0 && bw < e && bw > last) {
               v += part[bw * kSlots + r];
               vu += part[bw * kSlots + ru];
