@@ -857,6 +857,15 @@ __device__ __forceinline__ float resid_load(const EmitInfo& E, int row) {
   return (E.flags & F_TAGOUT) ? untag(r) : r;
 }
 
+// The residual as loaded (still tagged where the buffer is), for a load issued well before its use:
+// nothing touches the value until resid_ready, so the load's round trip overlaps the step's compute.
+__device__ __forceinline__ float resid_load_raw(const EmitInfo& E, int row) {
+  return (E.flags & F_RESID) ? ld_cg_f(out_ptr(E, row)) : 0.0f;
+}
+__device__ __forceinline__ float resid_ready(const EmitInfo& E, float raw) {
+  return (E.flags & F_TAGOUT) ? untag(raw) : raw;
+}
+
 __device__ __forceinline__ void emit(const EmitInfo& E, const EngParams& P, int row, float v, float v_up, float& wbv,
                                      int& wbi, float res) {
   if (E.pair) {
@@ -1353,7 +1362,7 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
       float res_pre = 0.0f;
       if (pl.split && (E.flags & F_RESID) && ctid < pl.ngroups * kSlots) {
         const int r0 = pl.r_lo + (ctid / kSlots) * g.U, r = ctid % kSlots;
-        if (r < (g.pair ? kSlots / 2 : kSlots) && r < min(g.U, pl.r_hi - r0)) res_pre = resid_load(E, r0 + r);
+        if (r < (g.pair ? kSlots / 2 : kSlots) && r < min(g.U, pl.r_hi - r0)) res_pre = resid_load_raw(E, r0 + r);
       }
       float* part = reinterpret_cast<float*>(smem + kOffPart);
       const int nout = g.pair ? kSlots / 2 : kSlots;  // output rows per group slot set
@@ -1424,12 +1433,16 @@ __global__ void __launch_bounds__(kThreads, 1) engine_kernel(const __grid_consta
           const int r0 = pl.r_lo + gi * g.U;
           if (r >= nout || r >= min(g.U, pl.r_hi - r0)) continue;
           const int ru = (r + kSlots / 2) % kSlots;  // the paired up row's slot (SwiGLU steps)
-          const float res = t == ctid ? res_pre : resid_load(E, r0 + r);
+          const float res = t == ctid ? resid_ready(E, res_pre) : resid_load(E, r0 + r);
           const int b0 = gi * g.nslab, e = b0 + g.nslab - 1;
           float v = 0.0f, vu = 0.0f;
           int last = -1;
+          int bws[kNumConsumerWarps - 1];
+#pragma unroll
+          for (int w = 0; w < kNumConsumerWarps - 1; ++w) bws[w] = wend[w];
+#pragma unroll
           for (int w = 0; w < kNumConsumerWarps - 1; ++w) {
-            const int bw = wend[w];
+            const int bw = bws[w];
             if (bw >= b0 && bw < e && bw > last) {
               v += part[bw * kSlots + r];
               vu += part[bw * kSlots + ru];
