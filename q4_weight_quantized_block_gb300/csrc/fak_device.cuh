@@ -211,3 +211,21 @@ int fak_bgemv_take_status();
 // while the stream is being captured into a graph, cudaMallocAsync (a graph
 // memory node).  Free with cudaFreeAsync on the same stream.
 cudaError_t fak_scratch_alloc(void** p, size_t bytes, cudaStream_t s);
+
+// Stream-K pieces of a prefill GEMM left to the caller's consumer instead of the fix-up kernel
+// (the prefill forward's residual add + RMSNorm sums them itself).  ws holds
+// [tiles][maxp][256 tokens][128 rows] f32 (tile t = row tile * n_tiles_p + token tile); the pieces
+// of tile t are those of the CTAs cf .. cl with cf = ((t nsb + 1) gs + work - 1) / work - 1 and
+// cl = ((t + 1) nsb gs + work - 1) / work - 1, summed in that order.  A tile met by one CTA was
+// written to Y.  ws == null: Y is complete.
+struct FakGemmPieces {
+  const float* ws;
+  int64_t work;  // tiles * nsb
+  int gs, nsb, maxp, n_tiles_p;
+};
+// Bytes of the pieces an N x K x P fak_q4k_gemm would cut (0 when it takes whole tiles).
+size_t fak_gemm_pieces_bytes(int64_t N, int64_t K, int64_t P);
+// fak_q4k_gemm, but a stream-K split leaves its pieces in ws (when ws_bytes holds them) and
+// describes them in *out; otherwise as fak_q4k_gemm, with out->ws = null.
+int fak_q4k_gemm_pieces(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, float* Y, float* ws,
+                        size_t ws_bytes, FakGemmPieces* out, fak_stream_t stream);

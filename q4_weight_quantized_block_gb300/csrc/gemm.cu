@@ -588,8 +588,60 @@ extern "C" int fak_swiglu_bf16(const float* Y1, int64_t P, int64_t half, void* X
 }
 
 namespace {
+// The work split of an N x K x P GEMM on `sms` SMs: whole tiles, or stream-K (see launch_gemm).
+struct SkPlan {
+  int tiles, nsb, n_tiles_p, gs, maxp;
+  int64_t work;
+  bool stream;
+};
+
+SkPlan plan_gemm(int64_t N, int64_t K, int64_t P, int sms, bool x2) {
+  SkPlan pl;
+  pl.n_tiles_p = (int)((P + BN - 1) / BN);
+  pl.tiles = (int)((N + BM - 1) / BM) * pl.n_tiles_p;
+  pl.nsb = (int)(K / 256);
+  // Stream-K when whole tiles fill the SMs poorly: the tiles' K work is cut into `sms` equal
+  // ranges, one per CTA, at super-block granularity.  Cost model in super-blocks of work on the
+  // critical path: whole tiles waves(tiles) * nsb; stream-K ceil(tiles * nsb / sms) +
+  // kStreamKFixCost, the constant standing for writing the pieces and the fix-up kernel that sums
+  // them; stream-K is taken below 0.85 x the whole-tile cost.  Both set by timing the two forms on
+  // the prefill shapes (P = 128 .. 1024): stream-K won by 2-3x where it costs under 0.65 x the whole
+  // tiles (down, out projections) and lost 0-8 % at 0.85-0.9 (gate||up, in_proj: several full
+  // waves of whole tiles).  Not with the SwiGLU epilogue, which needs whole
+  // tiles (so the fused gate||up GEMM equals the unfused one bit for bit when the unfused takes
+  // whole tiles).
+  pl.work = (int64_t)pl.tiles * pl.nsb;
+  pl.gs = (int)std::min<int64_t>(sms, pl.work);  // stream-K CTAs: every range at least one super-block
+  const double whole = (double)((pl.tiles + sms - 1) / sms) * pl.nsb;
+  const double streamk = (double)((pl.work + pl.gs - 1) / pl.gs) + kStreamKFixCost;
+  pl.stream = !x2 && streamk < 0.85 * whole;
+  pl.maxp = 1;
+  if (pl.stream) {
+    // the most pieces any tile is cut into (CTA c's range starts at floor(c work / sms))
+    for (int t = 0; t < pl.tiles; ++t) {
+      const int64_t tb = (int64_t)t * pl.nsb, te = tb + pl.nsb;
+      const int64_t cf = ((tb + 1) * pl.gs + pl.work - 1) / pl.work - 1, cl = (te * pl.gs + pl.work - 1) / pl.work - 1;
+      pl.maxp = std::max<int>(pl.maxp, (int)(cl - cf + 1));
+    }
+  }
+  return pl;
+}
+
+size_t pieces_bytes(const SkPlan& pl) {
+  return pl.stream && pl.maxp > 1 ? (size_t)pl.tiles * pl.maxp * BM * BN * 4 : 0;
+}
+
+// ext_ws / out: the pieces of a stream-K split go to the caller's workspace (ext_ws_bytes must hold
+// them) and *out describes them; no fix-up kernel runs, and the tiles cut into pieces are not
+// written to Y.
 int launch_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, float* Y, __nv_bfloat16* x2,
-                fak_stream_t stream_arg) {
+                fak_stream_t stream_arg, float* ext_ws = nullptr, size_t ext_ws_bytes = 0,
+                FakGemmPieces* out = nullptr) {
+  if (out) {
+    out->ws = nullptr;
+    out->work = 0;
+    out->gs = out->nsb = out->maxp = out->n_tiles_p = 0;
+  }
   if (K < 256 || K % 256 || N < 1 || N > (1LL << 31) - 1 || P < 1 || P > (1LL << 31) - 1 || K > (1LL << 31) - 1)
     return FAK_ERR_SHAPE;
   if ((reinterpret_cast<uintptr_t>(Wq) & 15) || (reinterpret_cast<uintptr_t>(X) & 15)) return FAK_ERR_ALIGN;
@@ -626,43 +678,31 @@ int launch_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, 
   gp.n_tiles_n = (int)((N + BM - 1) / BM);  // a last partial tile reads zero-filled rows past N, writes none
   gp.n_tiles_p = (int)((P + BN - 1) / BN);
   gp.timeout_ns = 2000000000ull;
-  const int tiles = gp.n_tiles_n * gp.n_tiles_p;
-  const int nsb = (int)(K / 256);
-  // Stream-K when whole tiles fill the SMs poorly: the tiles' K work is cut into `sms` equal
-  // ranges, one per CTA, at super-block granularity.  Cost model in super-blocks of work on the
-  // critical path: whole tiles waves(tiles) * nsb; stream-K ceil(tiles * nsb / sms) +
-  // kStreamKFixCost, the constant standing for writing the pieces and the fix-up kernel that sums
-  // them; stream-K is taken below 0.85 x the whole-tile cost.  Both set by timing the two forms on
-  // the prefill shapes (P = 128 .. 1024): stream-K won by 2-3x where it costs under 0.65 x the whole
-  // tiles (down, out projections) and lost 0-8 % at 0.85-0.9 (gate||up, in_proj: several full
-  // waves of whole tiles).  Not with the SwiGLU epilogue, which needs whole
-  // tiles (so the fused gate||up GEMM equals the unfused one bit for bit when the unfused takes
-  // whole tiles).
-  const int64_t work = (int64_t)tiles * nsb;
-  const int gs = (int)std::min<int64_t>(sms, work);  // stream-K CTAs: every range at least one super-block
-  const double whole = (double)((tiles + sms - 1) / sms) * nsb;
-  const double streamk = (double)((work + gs - 1) / gs) + kStreamKFixCost;
-  const bool stream = !x2 && streamk < 0.85 * whole;
+  const SkPlan pl = plan_gemm(N, K, P, sms, x2 != nullptr);
+  const int tiles = pl.tiles, nsb = pl.nsb, gs = pl.gs;
+  const int64_t work = pl.work;
+  const bool stream = pl.stream;
   gp.splits = 1;
   gp.sb_per = nsb;
   gp.stream = stream ? 1 : 0;
   gp.nsb = nsb;
-  gp.maxp = 1;
-  if (stream) {
-    // the most pieces any tile is cut into (CTA c's range starts at floor(c work / sms))
-    for (int t = 0; t < tiles; ++t) {
-      const int64_t tb = (int64_t)t * nsb, te = tb + nsb;
-      const int64_t cf = ((tb + 1) * gs + work - 1) / work - 1, cl = (te * gs + work - 1) / work - 1;
-      gp.maxp = std::max<int>(gp.maxp, (int)(cl - cf + 1));
-    }
-  }
+  gp.maxp = pl.maxp;
   gp.x2 = x2;
   gp.F = N / 2;
   gp.ws = nullptr;
   cudaStream_t s = (cudaStream_t)stream_arg;
   void* buf = nullptr;
-  const bool fixup = stream && gp.maxp > 1;
-  if (fixup) {
+  bool fixup = stream && gp.maxp > 1;
+  if (fixup && out && ext_ws && ext_ws_bytes >= pieces_bytes(pl)) {
+    gp.ws = ext_ws;
+    out->ws = ext_ws;
+    out->work = work;
+    out->gs = gs;
+    out->nsb = nsb;
+    out->maxp = gp.maxp;
+    out->n_tiles_p = gp.n_tiles_p;
+    fixup = false;
+  } else if (fixup) {
     const size_t ws_bytes = (size_t)tiles * gp.maxp * BM * BN * 4;
     const cudaError_t e = fak_scratch_alloc(&buf, ws_bytes, s);
     if (e != cudaSuccess) {
@@ -696,6 +736,18 @@ extern "C" int fak_q4k_gemm(const void* Wq, int64_t N, int64_t K, const void* X,
                             fak_stream_t stream) {
   if (!Wq || !X || !Y) return FAK_ERR_INVALID_ARG;
   return launch_gemm(Wq, N, K, X, P, Y, nullptr, stream);
+}
+
+size_t fak_gemm_pieces_bytes(int64_t N, int64_t K, int64_t P) {
+  int sms = 0;
+  if (K < 256 || K % 256 || N < 1 || P < 1 || gemm_setup(&sms) != FAK_OK) return 0;
+  return pieces_bytes(plan_gemm(N, K, P, sms, false));
+}
+
+int fak_q4k_gemm_pieces(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, float* Y, float* ws,
+                        size_t ws_bytes, FakGemmPieces* out, fak_stream_t stream) {
+  if (!Wq || !X || !Y || !out) return FAK_ERR_INVALID_ARG;
+  return launch_gemm(Wq, N, K, X, P, Y, nullptr, stream, ws, ws_bytes, out);
 }
 
 extern "C" int fak_q4k_gemm_swiglu(const void* W13, int64_t F, int64_t K, const void* X, int64_t P, void* X2,

@@ -59,11 +59,25 @@ __device__ __forceinline__ float row_sum(float v, float* scr) {
 }
 
 // Row p: optionally h += y (the residual add of the previous matmul), then
-// n = bf16(h / sqrt(mean(h^2) + eps)).  D % 4 == 0, D <= 8 * 4 * kRowThreads.
-__global__ void __launch_bounds__(kRowThreads) add_rms_bf16_kernel(float* h, const float* y, int D, float eps,
-                                                                   __nv_bfloat16* n) {
+// n = bf16(h / sqrt(mean(h^2) + eps)).  D % 128 == 0, D <= 8 * 4 * kRowThreads.
+// When pc.ws is set, y came from a stream-K GEMM whose cut tiles were left as pieces: the columns of
+// such a tile are the sum of its pieces in K order (as the GEMM's own fix-up would sum them), read
+// here instead of y; the other tiles were written to y.
+__global__ void __launch_bounds__(kRowThreads) add_rms_bf16_kernel(float* h, const float* y, const FakGemmPieces pc,
+                                                                   int D, float eps, __nv_bfloat16* n) {
   __shared__ float scr[kRowThreads / 32];
-  const int64_t off = (int64_t)blockIdx.x * D;
+  __shared__ int npc[64];  // pieces of each 128-row tile in this token's tile column
+  const int64_t p = blockIdx.x, off = p * D;
+  const int pt = (int)(p / 256), col = (int)(p % 256);
+  if (y && pc.ws) {
+    for (int j = threadIdx.x; j < D / 128; j += kRowThreads) {
+      const int64_t t = (int64_t)j * pc.n_tiles_p + pt;
+      const int64_t tb = t * pc.nsb, te = tb + pc.nsb;
+      const int64_t cf = ((tb + 1) * pc.gs + pc.work - 1) / pc.work - 1, cl = (te * pc.gs + pc.work - 1) / pc.work - 1;
+      npc[j] = (int)(cl - cf + 1);
+    }
+    __syncthreads();
+  }
   float4 v[8];
   float ss = 0.0f;
 #pragma unroll
@@ -72,7 +86,22 @@ __global__ void __launch_bounds__(kRowThreads) add_rms_bf16_kernel(float* h, con
     if (i < D / 4) {
       v[k] = reinterpret_cast<const float4*>(h + off)[i];
       if (y) {
-        const float4 r = reinterpret_cast<const float4*>(y + off)[i];
+        const int j = i >> 5, q = 4 * (i & 31);  // 128-row tile of these four columns, and the row in it
+        float4 r;
+        if (pc.ws && npc[j] > 1) {
+          const float4* src = reinterpret_cast<const float4*>(
+              pc.ws + (((int64_t)j * pc.n_tiles_p + pt) * pc.maxp * 256 + col) * 128 + q);
+          r = __ldcg(src);
+          for (int kk = 1; kk < npc[j]; ++kk) {
+            const float4 u = __ldcg(src + (int64_t)kk * (256 * 128 / 4));
+            r.x += u.x;
+            r.y += u.y;
+            r.z += u.z;
+            r.w += u.w;
+          }
+        } else {
+          r = reinterpret_cast<const float4*>(y + off)[i];
+        }
         v[k].x += r.x;
         v[k].y += r.y;
         v[k].z += r.z;
@@ -180,6 +209,8 @@ struct fak_prefill {
   float* T = nullptr;              // [P, max(gdn_in, fa_qg + 2 fa_kv)]
   __nv_bfloat16* X2 = nullptr;     // [P, max(n_mix, d_ff)]
   float* Y = nullptr;              // [P, D]
+  float* ws = nullptr;             // stream-K pieces of the out_proj / o and down GEMMs, summed by add+RMSNorm
+  size_t ws_bytes = 0;
   float* nlast = nullptr;          // [D]
   float* logits = nullptr;         // [vocab]
   unsigned long long* slot = nullptr;
@@ -205,6 +236,7 @@ void free_prefill(fak_prefill* c) {
   cudaFree(c->T);
   cudaFree(c->X2);
   cudaFree(c->Y);
+  cudaFree(c->ws);
   cudaFree(c->nlast);
   cudaFree(c->logits);
   cudaFree(c->slot);
@@ -223,6 +255,7 @@ int record_forward(fak_prefill* c, cudaStream_t s) {
   embed_rows_kernel<<<(unsigned)P, kRowThreads, 0, s>>>(c->toks, d.embedding, d.vocab, D, c->h);
   if ((st = launch_status(cudaSuccess)) != FAK_OK) return st;
   const float* pending = nullptr;  // a matmul output still to be added into h
+  FakGemmPieces pend_pc{};         // ... and its stream-K pieces, if it left them
   for (int l = 0; l < d.n_layers; ++l) {
     const fak_layer_desc& L = c->layers[l];
     // FA: q+gate, k and v share their input, so they run as one GEMM on the concatenated copy
@@ -230,16 +263,26 @@ int record_forward(fak_prefill* c, cudaStream_t s) {
     // is left out)
     const bool fa = L.kind == FAK_LAYER_FA;
     const int64_t nin = fa ? d.fa_qg + 2 * d.fa_kv : d.gdn_in;
-    add_rms_bf16_kernel<<<(unsigned)P, kRowThreads, 0, s>>>(c->h, pending, D, d.eps, c->n);
+    add_rms_bf16_kernel<<<(unsigned)P, kRowThreads, 0, s>>>(c->h, pending, pend_pc, D, d.eps, c->n);
     if ((st = launch_status(cudaSuccess)) != FAK_OK) return st;
     if ((st = fak_q4k_gemm(fa ? c->wqkv[l] : L.w_in, nin, D, c->n, P, c->T, s)) != FAK_OK) return st;
     slice_bf16_kernel<<<(unsigned)P, kRowThreads, 0, s>>>(c->T, nin, d.n_mix, c->X2);
     if ((st = launch_status(cudaSuccess)) != FAK_OK) return st;
-    if ((st = fak_q4k_gemm(L.w_out, D, d.n_mix, c->X2, P, c->Y, s)) != FAK_OK) return st;
-    add_rms_bf16_kernel<<<(unsigned)P, kRowThreads, 0, s>>>(c->h, c->Y, D, d.eps, c->n);
+    // the residual add + RMSNorm that follows sums the GEMM's stream-K pieces itself: no fix-up
+    // kernel, no round trip of the cut tiles through Y
+    FakGemmPieces pc{};
+    if ((st = fak_q4k_gemm_pieces(L.w_out, D, d.n_mix, c->X2, P, c->Y, c->ws, c->ws_bytes, &pc, s)) != FAK_OK)
+      return st;
+    add_rms_bf16_kernel<<<(unsigned)P, kRowThreads, 0, s>>>(c->h, c->Y, pc, D, d.eps, c->n);
     if ((st = launch_status(cudaSuccess)) != FAK_OK) return st;
     if ((st = fak_q4k_gemm_swiglu(c->w13[l], F, D, c->n, P, c->X2, s)) != FAK_OK) return st;
-    if ((st = fak_q4k_gemm(L.w_down, D, F, c->X2, P, c->Y, s)) != FAK_OK) return st;
+    // the last layer's output goes to the all-rows add, which reads Y only
+    pend_pc = FakGemmPieces{};
+    if (l + 1 < d.n_layers)
+      st = fak_q4k_gemm_pieces(L.w_down, D, F, c->X2, P, c->Y, c->ws, c->ws_bytes, &pend_pc, s);
+    else
+      st = fak_q4k_gemm(L.w_down, D, F, c->X2, P, c->Y, s);
+    if (st != FAK_OK) return st;
     pending = c->Y;
   }
   if (pending) {
@@ -291,6 +334,8 @@ extern "C" int fak_prefill_create(const fak_decode_desc* d, int64_t P, fak_prefi
             cudaMalloc(&c->Y, P * D * 4) == cudaSuccess && cudaMalloc(&c->nlast, D * 4) == cudaSuccess &&
             cudaMalloc(&c->logits, (size_t)d->vocab * 4) == cudaSuccess &&
             cudaMalloc(&c->slot, sizeof(unsigned long long)) == cudaSuccess && cudaMalloc(&c->tok, 4) == cudaSuccess;
+  c->ws_bytes = std::max(fak_gemm_pieces_bytes(D, d->n_mix, P), fak_gemm_pieces_bytes(D, F, P));
+  if (ok && c->ws_bytes) ok = cudaMalloc(&c->ws, c->ws_bytes) == cudaSuccess;
   const size_t w13_bytes = (size_t)(2 * F) * (D / 256) * 144;
   const size_t row_bytes = (size_t)(D / 256) * 144;
   for (int l = 0; ok && l < d->n_layers; ++l) {
