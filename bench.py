@@ -613,9 +613,9 @@ def bench_components(fak, torch, hbm, bf16, which):
 
 
 # dram bytes (read + write) of one full decode launch: the ncu capture of the same engine kernel on the
-# 4-layer stack (956.66 MB for 945.22 MB of weights), scaled by weight bytes to the 15.048 GB step.
+# 4-layer stack (955.81 MB for 945.22 MB of weights), scaled by weight bytes to the 15.048 GB step.
 # Set to None whenever the engine kernel changes until re-captured.
-DECODE_TRAFFIC_BYTES = int(956.661504e6 / 945.22368e6 * (15_048_048_640 + 5120 * 4))
+DECODE_TRAFFIC_BYTES = int(955.814144e6 / 945.22368e6 * (15_048_048_640 + 5120 * 4))
 
 
 def main():
