@@ -77,6 +77,25 @@ def test_gemm_deterministic(fak, N, K, P):
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
+@pytest.mark.parametrize("N,K,P", [(34816, 5120, 512), (5120, 17408, 512), (5120, 6144, 256)])
+def test_gemm_deterministic_full_shape(fak, N, K, P):
+    # the prefill shapes (whole tiles; stream-K with the fix-up): repeated calls agree bit for bit,
+    # so every producer / consumer hand-off of the pipeline is ordered (a reader that ran ahead of a
+    # ring slot's refill would read stale quants in some calls and not in others)
+    w = torch.empty(N * K, device="cuda")
+    synth.normal_device(w, 44, 0, 0.02)
+    Wg = torch.empty(N * K // 256 * 144, dtype=torch.uint8, device="cuda")
+    fak.fak_q4k_pack_device(w, N, K, Wg)
+    xf = torch.empty(P * K, device="cuda")
+    synth.normal_device(xf, 44, 1, 1.0)
+    Xb = xf.view(P, K).to(torch.bfloat16).view(torch.int16)
+    del w, xf
+    ref = gemm(fak, Wg, N, K, Xb, P)
+    assert torch.isfinite(ref).all()
+    for _ in range(4):
+        assert torch.equal(gemm(fak, Wg, N, K, Xb, P).view(torch.int32), ref.view(torch.int32))
+
+
 def test_swiglu_bf16(fak):
     P, half = 5, 1000
     Y1 = synth.normal(43, 0, (P, 2 * half), 3.0)
