@@ -402,6 +402,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         y[mm] = fmaf(d * iv[m], dot, y[mm]);
         y[mm] = fmaf(-dmin, ms, y[mm]);
       }
+      // the record's loads are complete (consumed above, and the fence waits for them) before the
+      // slot can be refilled by the next bulk copy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[s]);
       return true;
@@ -424,8 +427,6 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       uint4 qv[2 * kG];
 #pragma unroll
       for (int c = 0; c < 2 * kG; ++c) qv[c] = *reinterpret_cast<const uint4*>(rowp + 16 + 32 * kG * kp + 16 * c);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&wempty[ws]);
 
       const int a = i % C::kNBuf, use = i / C::kNBuf;
       if (use >= 1 && !mbar_wait_bounded(&cfull[a], (use - 1) & 1, abort, tmo)) {
@@ -456,7 +457,13 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       tmem_wait_st();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&afull[a]);
+      // the W slot is released only once its loads have fed the TMEM stores: an arrive right after
+      // the loads let the slot's TMA refill land before loads still in flight (seen in the prefill
+      // GEMM's per-step W ring)
+      if (lane == 0) {
+        mbar_arrive(&afull[a]);
+        mbar_arrive(&wempty[ws]);
+      }
       if (i >= C::kLag && !epilogue(i - C::kLag, hq[C::kLag - 1])) {
         ok = false;
         break;

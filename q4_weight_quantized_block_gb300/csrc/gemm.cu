@@ -6,15 +6,19 @@
 // mlp_down_proj take 73% of prefill; section 4b: the q4k_gemm prefill kernel).
 //
 // One CTA per SM, persistent over output tiles of 128 weight rows x 256 tokens,
-// K in steps of 64 through a 3-stage shared-memory pipeline:
+// K in steps of 64 through a 4-stage shared-memory pipeline:
 //   warp 0      TMA producer: X tile [256 tokens x 64] bf16, 128-byte swizzle
 //   warp 1      TMEM owner + MMA issuer: 4 x tcgen05.mma (M128 N256 K16) per stage
-//   warps 2-5   dequant producers: 128 W rows x 64 weights -> bf16, written in the
-//               same 128-byte-swizzled K-major layout (one thread per row, reading
-//               its row's Q4_K block from the W ring in shared memory)
+//   warps 2-5   dequant producers of the even K steps, warps 11-14 of the odd ones:
+//   and 11-14   128 W rows x 64 weights -> bf16, written in the same 128-byte-swizzled
+//               K-major layout (one thread per row, reading its row's Q4_K header and
+//               quants from the W ring in shared memory); two producer warps per
+//               scheduler, so one's waits and hand-offs hide under the other's arithmetic
 //   warps 6-9   epilogue: tcgen05.ld of the f32 accumulator -> Y (coalesced)
-//   warp 10     TMA producer (W): the 128-row x 144-byte Q4_K tile of each
-//               super-block into a two-slot ring, two super-blocks ahead
+//   warp 10     TMA producer (W): per super-block the 128 rows' 16-byte block headers
+//               into a two-slot ring, per K step the rows' 32 quant bytes of the step
+//               into a six-slot ring (an even count: a slot always serves the same
+//               producer warps, which wait on each of its phases in order)
 // Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile overlap
 // the MMAs of the next.  Every wait is bounded; on a timeout the kernel records
 // FAK_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
@@ -36,20 +40,26 @@ namespace {
 constexpr int BM = 128;  // weight rows per tile (MMA M)
 constexpr int BN = 256;  // tokens per tile (MMA N)
 constexpr int BK = 64;   // K per stage (one 128-byte swizzle atom of bf16)
-constexpr int kStagesG = 3;
-constexpr int kThreadsG = 352;
+constexpr int kStagesG = 4;
+constexpr int kThreadsG = 480;
 constexpr double kStreamKFixCost = 3.0;  // stream-K's extra cost, in super-block steps of one tile
-constexpr int kWSlots = 2;                // W super-block tiles in flight
-constexpr int kWTile = 128 * 144;       // 128 rows x 144 bytes
+constexpr int kWSlots = 6;                // quant slots in flight (one per K step; even)
+constexpr int kWTile = 128 * 32;          // 128 rows x the step's 32 quant bytes
+constexpr int kHSlots = 2;                // header slots (one per super-block)
+constexpr int kHTile = 128 * 16;          // 128 rows x 16-byte block header
 constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kBBytes = BN * BK * 2;  // 32 KB
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kStagesG * kABytes;
 constexpr int kOffW = kOffB + kStagesG * kBBytes;
-constexpr int kOffBarG = kOffW + kWSlots * kWTile;
-constexpr int kSmemG = kOffBarG + 256;
+constexpr int kOffH = kOffW + kWSlots * kWTile;
+constexpr int kOffBarG = kOffH + kHSlots * kHTile;
+constexpr int kSmemG = kOffBarG + 512;
 constexpr int kSmemAllocG = kSmemG + 1024;
 constexpr uint32_t kTmemCols = 512;
+static_assert(kSmemAllocG <= 232448, "GEMM shared memory exceeds the 227 KB per-block limit");
+static_assert((2 * kStagesG + 5 + 2 * kWSlots + 2 * kHSlots) * 8 + 8 <= 512, "GEMM barriers exceed their area");
+static_assert(kWSlots % 2 == 0 && kStagesG % 2 == 0, "each ring slot must serve one parity of K steps");
 
 __device__ int g_gemm_status;
 
@@ -233,25 +243,26 @@ FAK_DEV float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
 __global__ void __launch_bounds__(kThreadsG, 1)
     q4k_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
-                    const __grid_constant__ GemmParams p) {
+                    const __grid_constant__ CUtensorMap qmap, const __grid_constant__ GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full_x = reinterpret_cast<uint64_t*>(smem + kOffBarG);
-  uint64_t* full_w = full_x + kStagesG;
-  uint64_t* empty = full_w + kStagesG;
+  // full[s]: stage s holds its X tile (TMA bytes) and its dequantized A tile (four warp arrivals)
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBarG);
+  uint64_t* empty = full + kStagesG;
   uint64_t* tfull = empty + kStagesG;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint64_t* wfull = drain + 1;
   uint64_t* wempty = wfull + kWSlots;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty + kWSlots);
+  uint64_t* hfull = wempty + kWSlots;
+  uint64_t* hempty = hfull + kHSlots;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(hempty + kHSlots);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesG; ++s) {
-      mbar_init(&full_x[s], 1);
-      mbar_init(&full_w[s], 4);
+      mbar_init(&full[s], 5);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -261,7 +272,11 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     mbar_init(drain, 1);
     for (int w = 0; w < kWSlots; ++w) {
       mbar_init(&wfull[w], 1);
-      mbar_init(&wempty[w], 4);
+      mbar_init(&wempty[w], 4);  // the four producer warps of the slot's K-step parity
+    }
+    for (int h = 0; h < kHSlots; ++h) {
+      mbar_init(&hfull[h], 1);
+      mbar_init(&hempty[h], 8);  // all eight producer warps
     }
     *abort = 0;
     fence_mbar_init();
@@ -301,15 +316,16 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             if (!*abort) fail();
             break;
           }
-          mbar_arrive_expect_tx(&full_x[s], kBBytes);
-          tma_load_2d(smem + kOffB + s * kBBytes, &xmap, kt * BK, p0, &full_x[s]);
+          mbar_arrive_expect_tx(&full[s], kBBytes);
+          tma_load_2d(smem + kOffB + s * kBBytes, &xmap, kt * BK, p0, &full[s]);
         }
       }
-      // let in-flight copies land before the CTA can exit
+      // let in-flight copies land before the CTA can exit (a stage's phase also takes the dequant
+      // warps' arrivals, which come in every run that did not abort; an abort waits out the bound)
       const int last = it;
       for (int q = last - kStagesG < 0 ? 0 : last - kStagesG; q < last; ++q) {
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(&full_x[q % kStagesG], (q / kStagesG) & 1))
+        while (!mbar_try_wait(&full[q % kStagesG], (q / kStagesG) & 1))
           if (globaltimer_ns() - t0 > 200000000ull) break;
       }
     }
@@ -333,7 +349,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         for (int kt = k0; kt < k1; ++kt, ++it) {
           const int s = it % kStagesG;
           const uint32_t ph = (it / kStagesG) & 1;
-          if (!mbar_wait_bounded(&full_x[s], ph, abort, tmo) || !mbar_wait_bounded(&full_w[s], ph, abort, tmo)) {
+          if (!mbar_wait_bounded(&full[s], ph, abort, tmo)) {
             if (!*abort) fail();
             ok = false;
             break;
@@ -355,36 +371,41 @@ __global__ void __launch_bounds__(kThreadsG, 1)
       while (!mbar_try_wait(drain, 0))
         if (globaltimer_ns() - t0 > 200000000ull) break;
     }
-  } else if (warp < 6) {
-    // ---------------- dequant producers: thread t owns row t of each W tile
-    const int t = threadIdx.x - 64;
+  } else if (warp < 6 || warp >= 11) {
+    // ---------------- dequant producers: thread t owns row t of each W tile; warps 2-5 take
+    // the even K steps (it counts the CTA's K steps), warps 11-14 the odd ones
+    const int par = warp >= 11 ? 1 : 0;
+    const int t = (warp - (par ? 11 : 2)) * 32 + lane;
     const int r8 = t & 7;
-    int it = 0, wq = 0;
+    int it = 0;
     bool ok = true;
     SegIter si;
     Seg sg;
     seg_begin(p, si);
     while (ok && !*abort && seg_next(p, si, sg)) {
       uint4 hdr = make_uint4(0, 0, 0, 0);
-      const uint8_t* rowp = nullptr;
       for (int kt = sg.k0; kt < sg.k1 && ok; ++kt, ++it) {
-        const int g = kt & 3;
-        if (g == 0) {
-          if (!mbar_wait_bounded(&wfull[wq % kWSlots], (wq / kWSlots) & 1, abort, tmo)) {
+        if ((it & 1) != par) continue;
+        const int g = kt & 3;  // segments hold whole super-blocks, so it and kt agree mod 4
+        if (g == par) {
+          // the warp's first step of the super-block (the CTA's (it / 4)-th): its rows' headers
+          const int hu = it >> 2, h = hu % kHSlots;
+          if (!mbar_wait_bounded(&hfull[h], (hu / kHSlots) & 1, abort, tmo)) {
             if (!*abort) fail();
             ok = false;
             break;
           }
-          rowp = smem + kOffW + (wq % kWSlots) * kWTile + t * 144;
-          hdr = *reinterpret_cast<const uint4*>(rowp);
+          hdr = *reinterpret_cast<const uint4*>(smem + kOffH + h * kHTile + t * 16);
         }
-        const uint4 q0 = *reinterpret_cast<const uint4*>(rowp + 16 + 32 * g);
-        const uint4 q1 = *reinterpret_cast<const uint4*>(rowp + 32 + 32 * g);
-        if (g == 3) {  // this super-block's W tile is fully read
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&wempty[wq % kWSlots]);
-          ++wq;
+        const int w = it % kWSlots;  // the quant ring advances one slot per K step, like the stages
+        if (!mbar_wait_bounded(&wfull[w], (it / kWSlots) & 1, abort, tmo)) {
+          if (!*abort) fail();
+          ok = false;
+          break;
         }
+        const uint8_t* slot = smem + kOffW + w * kWTile;
+        const uint4 q0 = *reinterpret_cast<const uint4*>(slot + t * 32);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(slot + t * 32 + 16);
         const int s = it % kStagesG;
         if (it >= kStagesG && !mbar_wait_bounded(&empty[s], ((it / kStagesG) - 1) & 1, abort, tmo)) {
           if (!*abort) fail();
@@ -395,7 +416,13 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         dequant_row_step(hdr, q0, q1, g, row_smem, r8);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full_w[s]);
+        if (lane == 0) {
+          mbar_arrive(&full[s]);
+          // the W slots are released only now: their loads fed the dequant's stores, which precede
+          // the fence, so no TMA refill can land before the reads
+          mbar_arrive(&wempty[w]);
+          if (g == par) mbar_arrive(&hempty[(it >> 2) % kHSlots]);
+        }
       }
     }
   } else if (warp < 10) {
@@ -457,26 +484,45 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
       const int nsb = (int)(p.K / 256);
-      int wq = 0;
+      int wq = 0, nh = 0;  // quant and header loads issued
       SegIter si;
       Seg sg;
       seg_begin(p, si);
       while (!*abort && seg_next(p, si, sg)) {
         const int row0 = (sg.tile / p.n_tiles_p) * BM;
-        for (int sb = sg.k0 / 4; sb < sg.k1 / 4 && sb < nsb; ++sb, ++wq) {
+        for (int kt = sg.k0; kt < sg.k1 && kt < 4 * nsb; ++kt, ++wq) {
+          if ((kt & 3) == 0) {
+            // super-block kt / 4 (the CTA's (wq / 4)-th): the rows' headers, bytes [144 sb, +16)
+            const int hu = wq >> 2, h = hu % kHSlots;
+            if (hu >= kHSlots && !mbar_wait_bounded(&hempty[h], ((hu / kHSlots) - 1) & 1, abort, tmo)) {
+              if (!*abort) fail();
+              break;
+            }
+            mbar_arrive_expect_tx(&hfull[h], kHTile);
+            tma_load_2d_hint(smem + kOffH + h * kHTile, &wmap, (kt >> 2) * 144, row0, &hfull[h], pol);
+            ++nh;
+          }
           const int w = wq % kWSlots;
           if (wq >= kWSlots && !mbar_wait_bounded(&wempty[w], ((wq / kWSlots) - 1) & 1, abort, tmo)) {
             if (!*abort) fail();
             break;
           }
+          // K step g of the super-block: the rows' quants, bytes [144 sb + 16 + 32 g, +32)
           mbar_arrive_expect_tx(&wfull[w], kWTile);
-          tma_load_2d_hint(smem + kOffW + w * kWTile, &wmap, sb * 144, row0, &wfull[w], pol);
+          tma_load_2d_hint(smem + kOffW + w * kWTile, &qmap, (kt >> 2) * 144 + 16 + 32 * (kt & 3), row0, &wfull[w],
+                           pol);
         }
         if (*abort) break;
       }
+      // let in-flight copies land before the CTA can exit
       for (int q = wq - kWSlots < 0 ? 0 : wq - kWSlots; q < wq; ++q) {
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(&wfull[q % kWSlots], (q / kWSlots) & 1))
+          if (globaltimer_ns() - t0 > 200000000ull) break;
+      }
+      for (int q = nh - kHSlots < 0 ? 0 : nh - kHSlots; q < nh; ++q) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&hfull[q % kHSlots], (q / kHSlots) & 1))
           if (globaltimer_ns() - t0 > 200000000ull) break;
       }
     }
@@ -658,14 +704,20 @@ int launch_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, 
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return FAK_ERR_CUDA;
-  // W as bytes [N rows, K/256*144]: one 128-row x 144-byte box per super-block
-  CUtensorMap wmap;
+  // W as bytes [N rows, K/256*144]: per K step a 128-row x 16-byte box of block headers and a
+  // 128-row x 32-byte box of the step's quants
+  CUtensorMap wmap, qmap;
   memset(&wmap, 0, sizeof(wmap));
+  memset(&qmap, 0, sizeof(qmap));
   const cuuint64_t row_bytes = (cuuint64_t)(K / 256) * 144;
   const cuuint64_t wdim[2] = {row_bytes, (cuuint64_t)N};
   const cuuint64_t wstride[1] = {row_bytes};
-  const cuuint32_t wbox[2] = {144, BM};
-  r = g_encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(Wq), wdim, wstride, wbox, estride,
+  const cuuint32_t hbox[2] = {16, BM}, qbox[2] = {32, BM};
+  r = g_encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(Wq), wdim, wstride, hbox, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return FAK_ERR_CUDA;
+  r = g_encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(Wq), wdim, wstride, qbox, estride,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return FAK_ERR_CUDA;
@@ -712,7 +764,7 @@ int launch_gemm(const void* Wq, int64_t N, int64_t K, const void* X, int64_t P, 
     gp.ws = static_cast<float*>(buf);
   }
   const int grid = stream ? gs : (tiles < sms ? tiles : sms);
-  q4k_gemm_kernel<<<grid, kThreadsG, kSmemAllocG, s>>>(map, wmap, gp);
+  q4k_gemm_kernel<<<grid, kThreadsG, kSmemAllocG, s>>>(map, wmap, qmap, gp);
   cudaError_t le = cudaGetLastError();
   if (fixup && le == cudaSuccess) {
     cudaLaunchConfig_t cfg;
