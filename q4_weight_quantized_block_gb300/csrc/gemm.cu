@@ -332,6 +332,9 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
+      // stage s's descriptors are stage 0's plus its offset (in 16-byte units; no carry out of the
+      // 14-bit address field, which holds the whole 227 KB)
+      const uint64_t ad0 = sw128_desc(smem_u32(smem + kOffA)), bd0 = sw128_desc(smem_u32(smem + kOffB));
       int it = 0, local = 0;
       SegIter si;
       Seg sg;
@@ -355,8 +358,8 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sw128_desc(smem_u32(smem + kOffA + s * kABytes));
-          const uint64_t bd = sw128_desc(smem_u32(smem + kOffB + s * kBBytes));
+          const uint64_t ad = ad0 + (uint64_t)((s * kABytes) >> 4);
+          const uint64_t bd = bd0 + (uint64_t)((s * kBBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             mma_bf16(dcol, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), (kt != k0) || (kk != 0));
