@@ -5,8 +5,9 @@ Bar: |err| <= 1e-5 * sum|w_i x_i| + 1e-6 per output and cosine >= 0.999999
 input-row bucket edge (1, 2, 8, 9, 16, 17, 32, 33, 64), ragged row tiles,
 split-K (few row tiles), one-super-block rows, awkward activations (zero rows,
 huge and tiny magnitudes, per-super-block scale jumps), degenerate super-blocks
-(all-zero, constant negative), determinism, and the gate projection of the MLP
-workload at M = 1, 8, 64 sampled by rows.
+(all-zero, constant negative), determinism, the gate projection of the MLP
+workload at M = 1, 8, 64 sampled by rows, and bit-for-bit repeats of the full gate
+shape at M = 2, 8, 16, 64.
 """
 import numpy as np
 import pytest
@@ -122,3 +123,27 @@ def test_batch_gate_workload_sampled(fak, gate_packed, M):
     rb = Wo.reshape(N, -1)[rows]
     Yref, A = oracle.gemv_batch_q4k(rb, len(rows), K, X)
     check_f32(Y[:, rows], Yref, A, "gate workload M=%d (sampled rows)" % M)
+
+
+@pytest.mark.parametrize("M", [2, 8, 16, 64])
+def test_batch_gate_workload_repeats_bitwise(fak, M):
+    # the full gate shape, repeated: every ring hand-off of the kernel (W tiles, x parts, S records,
+    # TMEM buffers) is ordered, so repeated calls agree bit for bit
+    N, K = 17408, 5120
+    w = torch.empty(N * K, device="cuda")
+    synth.normal_device(w, 45, 0, 0.02)
+    Wg = torch.empty(N * K // 256 * 144, dtype=torch.uint8, device="cuda")
+    fak.fak_q4k_pack_device(w, N, K, Wg)
+    del w
+    X = torch.empty(M * K, device="cuda")
+    synth.normal_device(X, 45, 1, 1.0)
+    Ys = []
+    for _ in range(6):
+        Y = torch.full((M, N), float("nan"), device="cuda")
+        fak.fak_q4k_gemv_batch(Wg, N, K, X, M, Y)
+        Ys.append(Y)
+    torch.cuda.synchronize()
+    assert fak.fak_device_status() == 0
+    assert torch.isfinite(Ys[0]).all()
+    for Y in Ys[1:]:
+        assert torch.equal(Y.view(torch.int32), Ys[0].view(torch.int32))
