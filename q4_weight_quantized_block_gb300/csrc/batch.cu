@@ -163,14 +163,17 @@ __global__ void __launch_bounds__(256) bgemv_split_kernel(const float* __restric
 // sc * q for the 8 weights of one 32-bit word of nibbles, as four fp16 pairs:
 // (1024 + q) is built from the nibble bits, and one fused fp16 multiply-add
 // (1024 + q) * sc - 1024 * sc gives sc * q exactly.  lo[0..1] are the low
-// nibbles of bytes (0,1), (2,3); hi[0..1] the high nibbles.
+// nibbles of bytes (0,1), (2,3); hi[0..1] the high nibbles, taken in place as
+// (1024 + 16 q) (no shift: 16 q sits in mantissa bits 4-7, and 1024 + 16 q <= 1264
+// is exact) with mul_h = sc / 16 and add_h = -64 sc, both exact in fp16 for
+// sc <= 63, so the single rounding again gives sc * q exactly.
 FAK_DEV void scq_word(uint32_t v, uint32_t mul_l, uint32_t add_l, uint32_t mul_h, uint32_t add_h, uint32_t& lo0,
                       uint32_t& lo1, uint32_t& hi0, uint32_t& hi1) {
   const uint32_t t0 = prmt(v, 0u, 0x4140u), t1 = prmt(v, 0u, 0x4342u);
   lo0 = hfma2_bits(lop3_and_or(t0, 0x000F000Fu, 0x64006400u), mul_l, add_l);
   lo1 = hfma2_bits(lop3_and_or(t1, 0x000F000Fu, 0x64006400u), mul_l, add_l);
-  hi0 = hfma2_bits(lop3_and_or(t0 >> 4, 0x000F000Fu, 0x64006400u), mul_h, add_h);
-  hi1 = hfma2_bits(lop3_and_or(t1 >> 4, 0x000F000Fu, 0x64006400u), mul_h, add_h);
+  hi0 = hfma2_bits(lop3_and_or(t0, 0x00F000F0u, 0x64006400u), mul_h, add_h);
+  hi1 = hfma2_bits(lop3_and_or(t1, 0x00F000F0u, 0x64006400u), mul_h, add_h);
 }
 
 FAK_DEV uint32_t half2_splat(float f) {
@@ -444,7 +447,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         const int gi = g & 1;
         const float scl = (float)((scw >> (16 * gi)) & 0xFF), sch = (float)((scw >> (16 * gi + 8)) & 0xFF);
         const uint32_t mul_l = half2_splat(scl), add_l = half2_splat(-1024.0f * scl);
-        const uint32_t mul_h = half2_splat(sch), add_h = half2_splat(-1024.0f * sch);
+        const uint32_t mul_h = half2_splat(sch * 0.0625f), add_h = half2_splat(-64.0f * sch);
         const uint32_t wv[8] = {qv[2 * gg].x,     qv[2 * gg].y,     qv[2 * gg].z,     qv[2 * gg].w,
                                 qv[2 * gg + 1].x, qv[2 * gg + 1].y, qv[2 * gg + 1].z, qv[2 * gg + 1].w};
         uint32_t out[32];
