@@ -264,6 +264,17 @@ def bench_decode(fak, torch, args, dist, rank, world):
     pm_ms = time_events(torch, lambda: ctx_pm.step(tok, tok), max(3, args.steps // 3))
     launches_pm = ctx_pm.launches_per_step()
     ctx_pm.close()
+    # and with the host waiting for every launch before the next (the pages' commit-and-wait per
+    # command buffer); the step returns only once the token has finished, so host time is exact
+    ctx_hw = fak.DecodeContext(D, F, args.vocab, GI, QG, KV, NM, layers, lm, emb,
+                               mode=fak.FAK_DECODE_PER_MATMUL_HOST_WAIT)
+    ctx_hw.step(tok, tok)
+    n_hw = 3
+    t0 = time.perf_counter()
+    for _ in range(n_hw):
+        ctx_hw.step(tok, tok)
+    hw_ms = (time.perf_counter() - t0) * 1e3 / n_hw
+    ctx_hw.close()
 
     # the int8-activation variant of the same step (Q4_K steps on int8 x), and how far its logits
     # move from the exact step's on one token
@@ -293,7 +304,7 @@ def bench_decode(fak, torch, args, dist, rank, world):
     e2e_ms = max_over_ranks(dist, torch, e2e_ms, "cuda")
     return {"ms": ms, "tok_s": replica_throughput(world, ms), "clocks": clk.summary(), "algo_bytes": algo_bytes,
             "e2e_tok_s": replica_throughput(world, e2e_ms), "per_matmul_ms": pm_ms,
-            "per_matmul_launches": launches_pm, "i8x_ms": i8_ms, "i8x_logits_cosine": i8_cos,
+            "per_matmul_launches": launches_pm, "host_wait_ms": hw_ms, "i8x_ms": i8_ms, "i8x_logits_cosine": i8_cos,
             "i8x_same_token": i8_same_tok, "extra": extra}
 
 
@@ -674,6 +685,9 @@ def main():
         "gpu_launches": args.steps,
         "per_matmul_mode": {"ms_per_step": dec["per_matmul_ms"], "tok_s": 1e3 / dec["per_matmul_ms"],
                             "launches_per_step": dec["per_matmul_launches"]},
+        "per_matmul_host_wait_mode": {"ms_per_step": dec["host_wait_ms"], "tok_s": 1e3 / dec["host_wait_ms"],
+                                      "launches_per_step": dec["per_matmul_launches"],
+                                      "timing": "host clock over 3 steps; every launch waited on"},
         "decode_with_mixer": dec["extra"].get("decode_with_mixer"),
         "prefill_forward": dec["extra"].get("prefill_forward"),
         "int8_activation_variant": {"ms_per_step": dec["i8x_ms"], "tok_s": 1e3 / dec["i8x_ms"],

@@ -254,9 +254,14 @@ int fak_q4k_interleave_gate_up(const void* Wg, const void* Wu, int64_t F, int64_
 enum { FAK_LAYER_GDN = 0, FAK_LAYER_FA = 1 };
 /* ONE_LAUNCH: the whole token is one cooperative launch; PER_MATMUL: one launch
  * per step.  The _I8X modes are the same launch shapes with every Q4_K step on
- * int8 activations (fak_q4k_gemv_i8x); the Q8_0 lm_head keeps the exact form. */
+ * int8 activations (fak_q4k_gemv_i8x); the Q8_0 lm_head keeps the exact form.
+ * PER_MATMUL_HOST_WAIT is PER_MATMUL with the host waiting for each launch to
+ * finish (cudaStreamSynchronize) before it issues the next: the shape of the
+ * pages' Metal path, one command buffer per matmul, each committed and waited
+ * on ("Mac Qwen3.6-27B Metal Q4_K perf diagnosis", TL;DR and section 4b).  It
+ * returns after the token has finished on the device. */
 enum { FAK_DECODE_ONE_LAUNCH = 0, FAK_DECODE_PER_MATMUL = 1, FAK_DECODE_ONE_LAUNCH_I8X = 2,
-       FAK_DECODE_PER_MATMUL_I8X = 3 };
+       FAK_DECODE_PER_MATMUL_I8X = 3, FAK_DECODE_PER_MATMUL_HOST_WAIT = 4 };
 
 typedef struct {
     int32_t kind;          /* FAK_LAYER_GDN or FAK_LAYER_FA */
@@ -274,7 +279,8 @@ typedef struct {
     int32_t d_model, d_ff, vocab;
     int32_t gdn_in, fa_qg, fa_kv, n_mix;
     float eps;
-    int32_t mode;                 /* FAK_DECODE_ONE_LAUNCH, _PER_MATMUL, _ONE_LAUNCH_I8X or _PER_MATMUL_I8X */
+    int32_t mode;                 /* FAK_DECODE_ONE_LAUNCH, _PER_MATMUL, _ONE_LAUNCH_I8X, _PER_MATMUL_I8X
+                                     or _PER_MATMUL_HOST_WAIT */
     const fak_layer_desc* layers; /* host array of n_layers; copied by fak_decode_create */
     const void* lm_head;          /* [vocab x d_model] Q8_0, device */
     const float* embedding;       /* [vocab x d_model] f32, device */

@@ -11,7 +11,7 @@ q4_weight_quantized_block_gb300.build.build()).
 import importlib
 
 __all__ = [
-    "FAK_DECODE_ONE_LAUNCH", "FAK_DECODE_PER_MATMUL", "FAK_DECODE_ONE_LAUNCH_I8X", "FAK_DECODE_PER_MATMUL_I8X", "FAK_ENGINE_MAX_K", "FAK_MLP_NOALLOC_MAX_FF", "FAK_LAYER_FA", "FAK_LAYER_GDN",
+    "FAK_DECODE_ONE_LAUNCH", "FAK_DECODE_PER_MATMUL", "FAK_DECODE_ONE_LAUNCH_I8X", "FAK_DECODE_PER_MATMUL_I8X", "FAK_DECODE_PER_MATMUL_HOST_WAIT", "FAK_ENGINE_MAX_K", "FAK_MLP_NOALLOC_MAX_FF", "FAK_LAYER_FA", "FAK_LAYER_GDN",
     "STATUS", "DecodeContext", "PrefillContext", "FakError", "LIB_PATH", "fak_decode_create", "fak_device_status",
     "fak_mlp_decode", "fak_mlp_decode_noalloc", "fak_mlp_workspace_bytes", "fak_q4k_gemm", "fak_q4k_gemm_swiglu",
     "fak_q4k_gemv", "fak_q4k_gemv_batch", "fak_q4k_gemv_i8x", "fak_q4k_interleave_gate_up",

@@ -19,6 +19,7 @@ FAK_ENGINE_MAX_K = 18432
 FAK_MLP_NOALLOC_MAX_FF = 18432
 FAK_LAYER_GDN, FAK_LAYER_FA = 0, 1
 FAK_DECODE_ONE_LAUNCH, FAK_DECODE_PER_MATMUL, FAK_DECODE_ONE_LAUNCH_I8X, FAK_DECODE_PER_MATMUL_I8X = 0, 1, 2, 3
+FAK_DECODE_PER_MATMUL_HOST_WAIT = 4
 
 P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
 

@@ -914,30 +914,6 @@ __device__ __forceinline__ float reduce4(const float (&acc)[kSlots], int lane) {
 // shared memory (free between the previous step's last CTA barrier and the next
 // step's x preparation).
 
-// Polls one tagged value until it carries `want`; false on abort or timeout.
-__device__ __forceinline__ bool poll1(const float* p, uint32_t want, float& v, const EngParams& P,
-                                      volatile int* abort) {
-  v = ld_relaxed_f(p);
-  if ((__float_as_uint(v) & 1u) == want) {
-    v = untag(v);
-    return true;
-  }
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-    __nanosleep(64);
-    v = ld_relaxed_f(p);
-    if ((__float_as_uint(v) & 1u) == want) {
-      v = untag(v);
-      return true;
-    }
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > P.timeout_ns) {
-      set_error(P, FAK_ERR_TIMEOUT, abort);
-      return false;
-    }
-  }
-}
-
 // Up to N tagged values at once: every load is in flight together, then only the stale ones are
 // read again until all carry their expected tag (bounded like every wait).  use[k] false: slot k
 // is skipped and v[k] left as it is.
@@ -1778,6 +1754,7 @@ struct fak_decode {
   int sms = 0;
   int mode = 0;    // FAK_DECODE_ONE_LAUNCH or FAK_DECODE_PER_MATMUL
   bool i8x = false;  // int8 activations for the Q4_K steps
+  bool host_wait = false;  // per-matmul launches, each waited on by the host
   int n_ops = 0;
   int n_fa = 0;
   EngOp* d_ops = nullptr;
@@ -1882,7 +1859,7 @@ unsigned tag_flip(const fak_decode* c) {
 extern "C" int fak_decode_create(const fak_decode_desc* d, fak_decode** out) {
   if (!d || !out || !d->layers || !d->lm_head || !d->embedding) return FAK_ERR_INVALID_ARG;
   *out = nullptr;
-  if (d->mode < FAK_DECODE_ONE_LAUNCH || d->mode > FAK_DECODE_PER_MATMUL_I8X) return FAK_ERR_INVALID_ARG;
+  if (d->mode < FAK_DECODE_ONE_LAUNCH || d->mode > FAK_DECODE_PER_MATMUL_HOST_WAIT) return FAK_ERR_INVALID_ARG;
   auto okdim = [](int64_t v) { return v >= 256 && v % 256 == 0 && v <= FAK_ENGINE_MAX_K; };
   if (d->n_layers < 0 || !okdim(d->d_model) || !okdim(d->d_ff) || !okdim(d->n_mix) || d->vocab < 1 ||
       d->gdn_in < 1 || d->fa_qg < 1 || d->fa_kv < 1)
@@ -1930,8 +1907,11 @@ extern "C" int fak_decode_create(const fak_decode_desc* d, fak_decode** out) {
   c->layers.assign(d->layers, d->layers + d->n_layers);
   c->desc.layers = c->layers.data();
   c->sms = sms;
-  c->mode = d->mode & 1;  // the _I8X modes are the two launch shapes with int8 activations
-  c->i8x = d->mode >= FAK_DECODE_ONE_LAUNCH_I8X;
+  // the _I8X modes are the two launch shapes with int8 activations; HOST_WAIT is PER_MATMUL with a
+  // host wait after every launch
+  c->host_wait = d->mode == FAK_DECODE_PER_MATMUL_HOST_WAIT;
+  c->mode = c->host_wait ? FAK_DECODE_PER_MATMUL : (d->mode & 1);
+  c->i8x = d->mode == FAK_DECODE_ONE_LAUNCH_I8X || d->mode == FAK_DECODE_PER_MATMUL_I8X;
   c->n_fa = n_fa;
   if (c->mode == FAK_DECODE_ONE_LAUNCH) {
     int dev = 0, coop = 0, per_sm = 0;
@@ -2161,6 +2141,10 @@ extern "C" int fak_decode_step(fak_decode* c, const int32_t* tok_in, int32_t* to
     P.sync = nullptr;
     int st = launch_engine(P, c->sms, false, s, c->i8x);
     if (st != FAK_OK) return st;
+    if (c->host_wait) {
+      st = fak_cuda_status(cudaStreamSynchronize(s));
+      if (st != FAK_OK) return st;
+    }
   }
   ++c->token;
   return FAK_OK;

@@ -235,8 +235,10 @@ def test_decode_one_launch_equals_per_matmul_bitwise(fak):
     args = (c["D"], c["F"], c["V"], c["gdn_in"], c["qg"], c["kv"], c["n_mix"], lg, lm, emb)
     a = decode_run(fak, fak.DecodeContext(*args, mode=0), [3, 1, 4, 1, 5], c["V"])
     b = decode_run(fak, fak.DecodeContext(*args, mode=1), [3, 1, 4, 1, 5], c["V"])
-    for (ta, la), (tb, lb) in zip(a, b):
-        assert ta == tb and np.array_equal(la.view(np.uint32), lb.view(np.uint32))
+    h = decode_run(fak, fak.DecodeContext(*args, mode=fak.FAK_DECODE_PER_MATMUL_HOST_WAIT), [3, 1, 4, 1, 5], c["V"])
+    for (ta, la), (tb, lb), (th, lh) in zip(a, b, h):
+        assert ta == tb == th and np.array_equal(la.view(np.uint32), lb.view(np.uint32))
+        assert np.array_equal(la.view(np.uint32), lh.view(np.uint32))
 
 
 def test_decode_free_running_matches_oracle(fak):
