@@ -126,3 +126,14 @@ def test_prefill_create_rejects_bad_shapes_before_any_device_call(fak):
         with pytest.raises(fak.FakError) as ei:
             fak.PrefillContext(256, 512, 300, 640, 512, 256, 256, [layer], ok_ptr, ok_ptr, n_tokens)
         assert ei.value.status == 2
+
+
+def test_decode_create_rejects_unknown_modes_before_any_device_call(fak):
+    ok_ptr = 1 << 20
+    layer = {"kind": fak.FAK_LAYER_GDN, "w_in": ok_ptr, "w_out": ok_ptr, "w_gate": ok_ptr, "w_up": ok_ptr,
+             "w_down": ok_ptr}
+    assert fak.FAK_DECODE_PER_MATMUL_HOST_WAIT == 4
+    for mode in (-1, 5):
+        with pytest.raises(fak.FakError) as ei:
+            fak.DecodeContext(256, 512, 300, 640, 512, 256, 256, [layer], ok_ptr, ok_ptr, mode=mode)
+        assert ei.value.status == 1, mode
